@@ -1,0 +1,476 @@
+"""Benchmark of the W8A8 block-FP8 linear layer on GB300.
+
+Workload (one "step"): a decode pass at M = 1 over the five dense-27B
+projection shapes (N, K) = (17408, 5120), (5120, 3072), (5120, 8704),
+(7168, 5120), (8192, 5120): for each shape, fp8_act_quant of the token's
+bf16 activations and fp8_block_gemm against that shape's E4M3 weights.
+Inputs are seeded synthetic tensors (weights N(0, 0.02), activations N(0, 1)
+with 0.1% x20 outliers), quantised by the library's own kernels before the
+timed region. The weights are kept in three rotating copies (684 MB in
+total, over 5x the 129 MB L2), so every step reads its weights from HBM.
+
+Printed JSON line (rank 0):
+  value      achieved HBM GB/s of the whole step (algorithmic bytes / time),
+             steps replayed as CUDA graphs, inputs resident in HBM
+  e2e        the same through the public API with the activations copied in
+             from pinned host memory and the outputs copied back every step
+  roofline   the block GEMM kernel against the measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle on the same workload (host cores)
+  sweep      us/call per shape at M = 1..8 (the no-cliff check), 64, 102
+             and 4096 (the last as TFLOP/s of FP8 tensor peak)
+
+`--impl reference` times the CPU oracle instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from block_scaled_fp8_act_gb300 import inputs  # noqa: E402
+
+G = 128
+METRIC = "us/call and achieved HBM GB/s (% of roofline) for block-FP8 GEMM at M=1-8"
+WORKLOAD = "decode M=1 over the five dense-27B projection shapes (act quant + block-FP8 GEMM per shape)"
+WEIGHT_COPIES = 3
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense FP8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+
+
+# ------------------------------------------------------------------ helpers
+def algorithmic_gemm_bytes(M: int, N: int, K: int) -> int:
+    """Bytes the block GEMM must move: weights + their scales, codes +
+    scales of the activations, and the bf16 output."""
+    KB, NB = K // G, (N + G - 1) // G
+    return N * K + 4 * NB * KB + M * K + 4 * M * KB + 2 * M * N
+
+
+def algorithmic_quant_bytes(M: int, K: int) -> int:
+    """bf16 in, E4M3 codes and fp32 scales out."""
+    return 2 * M * K + M * K + 4 * M * (K // G)
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """Short hash of the CUDA sources, to tell whether recorded ncu traffic is current."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_scaled_fp8_act_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch recorded from an ncu capture for the current
+    sources (profiles/ncu_traffic.txt: `kernel workload source_hash bytes`)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    for line in open(path, encoding="utf-8"):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload \
+                and parts[2] == want:
+            return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during a timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workload
+class Weights:
+    """E4M3 weights + scales of the five shapes in `copies` rotating copies
+    (quantised on the device by fp8_weight_quant)."""
+
+    def __init__(self, device: torch.device, copies: int = WEIGHT_COPIES, shapes=inputs.SHAPES):
+        from block_scaled_fp8_act_gb300 import fp8act
+        self.shapes = list(shapes)
+        self.copies = copies
+        self.w, self.sw = [], []
+        for si, (N, K) in enumerate(self.shapes):
+            W = inputs.weights_bf16(N, K, inputs.weight_seed(si)).to(device)
+            w0, sw0 = fp8act.fp8_weight_quant(W)
+            del W
+            self.w.append([w0] + [w0.clone() for _ in range(copies - 1)])
+            self.sw.append([sw0] + [sw0.clone() for _ in range(copies - 1)])
+        torch.cuda.synchronize()
+
+
+class Workload:
+    """Device-resident activations of one M over the five shapes (plus pinned
+    host copies for the end-to-end leg), sharing one Weights set."""
+
+    def __init__(self, M: int, weights: Weights, device: torch.device):
+        self.M = M
+        self.shapes = weights.shapes
+        self.copies = weights.copies
+        self.w, self.sw = weights.w, weights.sw
+        self.x, self.q, self.sa, self.out = [], [], [], []
+        self.x_host, self.out_host = [], []
+        for si, (N, K) in enumerate(self.shapes):
+            x = inputs.activations_bf16(M, K, inputs.activation_seed(si, 0))
+            self.x_host.append(x.pin_memory())
+            self.x.append(x.to(device))
+            self.q.append(torch.empty((M, K), dtype=torch.uint8, device=device))
+            self.sa.append(torch.empty((M, K // G), dtype=torch.float32, device=device))
+            self.out.append(torch.empty((M, N), dtype=torch.bfloat16, device=device))
+            self.out_host.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
+        torch.cuda.synchronize()
+
+    def step_bytes(self) -> int:
+        return sum(algorithmic_gemm_bytes(self.M, N, K) + algorithmic_quant_bytes(self.M, K)
+                   for N, K in self.shapes)
+
+    def gemm_bytes(self) -> int:
+        return sum(algorithmic_gemm_bytes(self.M, N, K) for N, K in self.shapes)
+
+    def enqueue_step(self, copy: int, stream) -> None:
+        from block_scaled_fp8_act_gb300 import fp8act
+        for si in range(len(self.shapes)):
+            fp8act.fp8_act_quant(self.x[si], self.q[si], self.sa[si], stream=stream)
+            fp8act.fp8_block_gemm(self.q[si], self.sa[si], self.w[si][copy], self.sw[si][copy],
+                                  self.out[si], stream=stream)
+
+
+def capture(fn, stream) -> torch.cuda.CUDAGraph:
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm the code path once outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    return g
+
+
+def time_graphs(graphs, steps: int, warmup: int, stream) -> float:
+    """Seconds per replay, replaying graphs round-robin, CUDA events on `stream`."""
+    for i in range(warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            graphs[i % len(graphs)].replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3 / steps
+
+
+def gemm_kernel_times(wl: Workload, stream, launches: int = 60, reps: int = 5) -> list[float]:
+    """Average duration (s) of one fp8_block_gemm launch per shape: a CUDA
+    graph of `launches` back-to-back calls over the rotating weight copies,
+    timed with events on the launching stream, median over `reps` replays."""
+    from block_scaled_fp8_act_gb300 import fp8act
+    out = []
+    for si in range(len(wl.shapes)):
+        def chain(si=si):
+            for i in range(launches):
+                c = i % wl.copies
+                fp8act.fp8_block_gemm(wl.q[si], wl.sa[si], wl.w[si][c], wl.sw[si][c], wl.out[si], stream=stream)
+        g = capture(chain, stream)
+        ts = []
+        for _ in range(reps):
+            ts.append(time_graphs([g], 1, 1, stream) / launches)
+        out.append(statistics.median(ts))
+        del g
+    return out
+
+
+# ----------------------------------------------------------- CPU oracle leg
+def oracle_step_time(budget_s: float = 12.0) -> dict:
+    """The CPU oracle on the same workload: act quant + exact block GEMM per
+    shape at M = 1, weights quantised by the oracle beforehand (untimed).
+    Repeats whole steps until `budget_s` of work has been timed."""
+    import oracle
+    prepared = []
+    for si, (N, K) in enumerate(inputs.SHAPES):
+        W = inputs.weights_bf16(N, K, inputs.weight_seed(si))
+        w, sw = oracle.weight_quant(inputs.bf16_bits(W))
+        x = inputs.bf16_bits(inputs.activations_bf16(1, K, inputs.activation_seed(si, 0)))
+        prepared.append((x, w, sw))
+    times = []
+    t_total = 0.0
+    while t_total < budget_s or not times:
+        t0 = time.perf_counter()
+        for x, w, sw in prepared:
+            q, sa = oracle.act_quant(x)
+            oracle.block_gemm(q, sa, w, sw)
+        dt = time.perf_counter() - t0
+        times.append(dt)
+        t_total += dt
+    step_bytes = sum(algorithmic_gemm_bytes(1, N, K) + algorithmic_quant_bytes(1, K) for N, K in inputs.SHAPES)
+    per_step = statistics.median(times)
+    return {"value": step_bytes / per_step / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds_per_step": per_step, "steps_timed": len(times),
+            "sample": f"{len(times)} full decode steps (M=1, all five shapes: act quant + exact int64/fp64 GEMM); "
+                      f"weight quantisation untimed"}
+
+
+# ----------------------------------------------------------------- runner
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world: int, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world: int, rank: int) -> None:
+    if rank != 0:
+        return
+    cb = oracle_step_time(budget_s=args.cpu_budget)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": cb["steps_timed"], "warmup": 0, "ms_per_step": cb["seconds_per_step"] * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "M": 1, "shapes": inputs.SHAPES},
+            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def sweep(weights, device, stream, peaks) -> dict:
+    """us/call of the block GEMM per shape at every workload M (outside the timed step)."""
+    res = {}
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    for M in (1, 2, 3, 4, 5, 6, 7, 8, 64, 102, 4096):
+        wl = Workload(M, weights, device)
+        ts = gemm_kernel_times(wl, stream, launches=30 if M <= 102 else 3, reps=3)
+        row = []
+        for (N, K), t in zip(wl.shapes, ts):
+            e = {"N": N, "K": K, "us": round(t * 1e6, 3)}
+            if M <= 102:
+                gbs = algorithmic_gemm_bytes(M, N, K) / t / 1e9
+                e["gbs"] = round(gbs, 1)
+                e["frac_hbm"] = round(gbs / hbm, 4)
+            else:
+                tf = 2.0 * M * N * K / t / 1e12
+                e["tflops"] = round(tf, 1)
+                e["frac_fp8"] = round(tf / fp8_peak, 4)
+            row.append(e)
+        res[str(M)] = row
+        del wl
+        torch.cuda.empty_cache()
+    return res
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work to time")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    from block_scaled_fp8_act_gb300 import fp8act
+    fp8act.load(build=True)
+    device = torch.device("cuda", torch.cuda.current_device())
+    peaks, peaks_kind = load_peaks()
+    stream = torch.cuda.Stream()
+
+    weights = Weights(device)
+    wl = Workload(1, weights, device)
+    graphs = [capture(lambda c=c: wl.enqueue_step(c, stream), stream) for c in range(wl.copies)]
+    launches_per_step = 2 * len(wl.shapes)
+
+    # ---- timed region: K steps of the whole path, graphs replayed back to back
+    for i in range(args.warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                graphs[i % len(graphs)].replay()
+            end.record(stream)
+        end.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        t_step = start.elapsed_time(end) / 1e3 / args.steps
+        # dominant kernel: the block GEMM, timed per shape on the same stream
+        gemm_ts = gemm_kernel_times(wl, stream)
+    t_step = max_over_ranks(world, t_step)
+    step_bytes = wl.step_bytes()
+    value = world * step_bytes / t_step / 1e9
+
+    # ---- e2e: public API, activations from pinned host, outputs back, every step
+    def e2e_step(c):
+        for si in range(len(wl.shapes)):
+            wl.x[si].copy_(wl.x_host[si], non_blocking=True)
+        wl.enqueue_step(c, stream)
+        for si in range(len(wl.shapes)):
+            wl.out_host[si].copy_(wl.out[si], non_blocking=True)
+    e2e_steps = max(50, args.steps // 10)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i % wl.copies)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        s0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i % wl.copies)
+        s1.record(stream)
+        s1.synchronize()
+        wall = (time.perf_counter() - t0) / e2e_steps
+    t_e2e = max(s0.elapsed_time(s1) / 1e3 / e2e_steps, wall)
+    t_e2e = max_over_ranks(world, t_e2e)
+    h2d = sum(x.numel() * 2 for x in wl.x_host)
+    d2h = sum(o.numel() * 2 for o in wl.out_host)
+
+    gemm_bytes = [algorithmic_gemm_bytes(1, N, K) for N, K in wl.shapes]
+    achieved = sum(gemm_bytes) / sum(gemm_ts) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    traffic = recorded_traffic("gemm_skinny_kernel", "decode_m1_mean_of_5")
+    per_shape = [{"N": N, "K": K, "us_per_call": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1),
+                  "frac": round(b / t / 1e9 / peak, 4)}
+                 for (N, K), t, b in zip(wl.shapes, gemm_ts, gemm_bytes)]
+
+    del graphs
+    torch.cuda.synchronize()
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 acc -> bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "shapes": [list(s) for s in wl.shapes],
+                   "l2": f"inputs larger than L2: {wl.copies} rotating weight copies "
+                         f"({wl.copies * sum(N * K for N, K in wl.shapes) / 1e6:.0f} MB), no flush",
+                   "graphs": "each step is one CUDA graph replay (10 kernels)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": per_shape,
+        "gpu_launches": args.steps * launches_per_step,
+        "roofline": {"bound": "hbm", "kernel": "gemm_skinny_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_kind": f"{peaks_kind} HBM copy bandwidth",
+                     "bytes_per_launch": sum(gemm_bytes) / len(gemm_bytes),
+                     "us_per_launch": round(sum(gemm_ts) / len(gemm_ts) * 1e6, 3)},
+        "e2e": {"value": round(world * step_bytes / t_e2e / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 5)},
+        "clocks": clk.summary(),
+    }
+    if not args.no_sweep and rank == 0:
+        del wl
+        torch.cuda.empty_cache()
+        result["sweep"] = sweep(weights, device, stream, peaks)
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = oracle_step_time(budget_s=args.cpu_budget)
+        result["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

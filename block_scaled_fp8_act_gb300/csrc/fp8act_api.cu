@@ -1,0 +1,130 @@
+// C ABI of libfp8act: argument checks, device checks, dispatch on M.
+// The contract of every function is documented in include/fp8act.h.
+#include <atomic>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/fp8act.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kGroup = 128;
+
+// Per-device facts looked up once: -1 = unknown, 0 = unsupported, else SM count.
+std::atomic<int> g_device_sms[kMaxDevices];
+std::atomic<bool> g_device_init[kMaxDevices];
+
+// SM count of the current device if it is a compute-capability 10.3 part, 0 otherwise.
+int current_device_sms(int* status) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        *status = FP8ACT_ERR_DEVICE;
+        return 0;
+    }
+    if (!g_device_init[dev].load(std::memory_order_acquire)) {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaGetLastError();
+        g_device_sms[dev].store((major == 10 && minor == 3) ? sms : 0, std::memory_order_relaxed);
+        g_device_init[dev].store(true, std::memory_order_release);
+    }
+    const int sms = g_device_sms[dev].load(std::memory_order_relaxed);
+    *status = sms > 0 ? FP8ACT_OK : FP8ACT_ERR_DEVICE;
+    return sms;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return FP8ACT_OK;
+    return FP8ACT_ERR_LAUNCH;
+}
+
+// K: positive multiple of 128; rows*K must fit in int64 and each of M, N, K in int.
+int check_k(int K) { return (K <= 0 || K % kGroup) ? FP8ACT_ERR_SHAPE : FP8ACT_OK; }
+
+int gemm_common(const void* q, const float* sa, const void* w, const float* sw, int M, int N, int K, void* out,
+                bool out_f32, void* stream) {
+    if (M < 0 || N < 0) return FP8ACT_ERR_SHAPE;
+    if (int st = check_k(K)) return st;
+    if (M == 0 || N == 0) return FP8ACT_OK;
+    if (!q || !sa || !w || !sw || !out) return FP8ACT_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(w, 16) || !aligned(out, 16) || !aligned(sa, 4) || !aligned(sw, 4))
+        return FP8ACT_ERR_ALIGN;
+    int st = FP8ACT_OK;
+    const int sms = current_device_sms(&st);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return launch_status(fp8act::launch_gemm_skinny(static_cast<const uint8_t*>(q), sa,
+                                                    static_cast<const uint8_t*>(w), sw, M, N, K, out, out_f32,
+                                                    sms, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8_act_quant(const void* x_bf16, int M, int K, void* q_e4m3, float* sa, void* stream) {
+    if (M < 0) return FP8ACT_ERR_SHAPE;
+    if (int st = check_k(K)) return st;
+    if (M == 0) return FP8ACT_OK;
+    if (!x_bf16 || !q_e4m3 || !sa) return FP8ACT_ERR_NULL;
+    if (!aligned(x_bf16, 16) || !aligned(q_e4m3, 16) || !aligned(sa, 4)) return FP8ACT_ERR_ALIGN;
+    int st = FP8ACT_OK;
+    const int sms = current_device_sms(&st);
+    if (st) return st;
+    return launch_status(fp8act::launch_act_quant(x_bf16, M, K, q_e4m3, sa, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_weight_quant(const void* w_bf16, int N, int K, void* w_e4m3, float* sw, void* stream) {
+    if (N < 0) return FP8ACT_ERR_SHAPE;
+    if (int st = check_k(K)) return st;
+    if (N == 0) return FP8ACT_OK;
+    if (!w_bf16 || !w_e4m3 || !sw) return FP8ACT_ERR_NULL;
+    if (!aligned(w_bf16, 16) || !aligned(w_e4m3, 16) || !aligned(sw, 4)) return FP8ACT_ERR_ALIGN;
+    int st = FP8ACT_OK;
+    current_device_sms(&st);
+    if (st) return st;
+    return launch_status(fp8act::launch_weight_quant(w_bf16, N, K, w_e4m3, sw, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_block_gemm(const void* q_e4m3, const float* sa, const void* w_e4m3, const float* sw, int M, int N, int K,
+                   void* out_bf16, void* stream) {
+    return gemm_common(q_e4m3, sa, w_e4m3, sw, M, N, K, out_bf16, false, stream);
+}
+
+int fp8_block_gemm_f32(const void* q_e4m3, const float* sa, const void* w_e4m3, const float* sw, int M, int N,
+                       int K, float* out_f32, void* stream) {
+    return gemm_common(q_e4m3, sa, w_e4m3, sw, M, N, K, out_f32, true, stream);
+}
+
+const char* fp8act_strerror(int status) {
+    switch (status) {
+        case FP8ACT_OK: return "ok";
+        case FP8ACT_ERR_NULL: return "a required pointer is NULL";
+        case FP8ACT_ERR_SHAPE: return "bad shape: M, N must be >= 0 and K a positive multiple of 128";
+        case FP8ACT_ERR_ALIGN: return "misaligned pointer: tensors need 16-byte, scales 4-byte alignment";
+        case FP8ACT_ERR_LAUNCH: return "kernel launch failed";
+        case FP8ACT_ERR_TIMEOUT: return "a kernel gave up a bounded wait (device-side timeout)";
+        case FP8ACT_ERR_DEVICE: return "no current CUDA device of compute capability 10.3 (GB300)";
+        case FP8ACT_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown fp8act status";
+    }
+}
+
+int fp8act_check_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8ACT_ERR_CUDA;
+    }
+    return FP8ACT_OK;
+}
+
+int fp8act_version(void) { return 100; }
+
+}  // extern "C"

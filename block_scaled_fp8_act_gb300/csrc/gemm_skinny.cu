@@ -1,0 +1,178 @@
+// Weight-streaming block-FP8 GEMM for small M (decode and speculative verify).
+//
+// At M <= 8 the layer is a pure weight stream: every weight byte is used for
+// at most 8 multiply-adds, so the kernel is bound by HBM. The pages put about
+// 89% of a decode step into exactly these weight-reading GEMMs and name a
+// library kernel that fell off a cliff between M = 1 and M = 2..7
+// ("单并发提速73%,多并发能力达原来2.4倍:Qwen3.8-27B性能优化实践", section
+// "算子优化"). This kernel has one code path for every M <= 8, so its time does
+// not depend on M.
+//
+// Why tensor cores for a memory-bound kernel: at M = 8 the CUDA cores would
+// need 8 fp32 FMAs per weight byte, i.e. ~190 FMA/clk/SM at the HBM rate,
+// above the 128 the SM has. One warp-level m16n8k32 e4m3 MMA does 16x8x32
+// multiply-adds, so the arithmetic costs a few instructions per 2 KB of
+// weights and the loads stay in front.
+//
+// Layout of the work:
+//  - A CTA owns a 16-row tile of W (rows n0..n0+15, all inside one 128-row
+//    scale block) and a group of <= 8 tokens. Its warps split the K blocks
+//    (kb = warp, warp + nwarps, ...), so each warp's partial sums are for
+//    whole 128-wide blocks and the fp32 block scales are applied in registers.
+//  - Swap-AB: the 16 weight rows are the MMA's A operand (m16), the tokens its
+//    B operand (n8), so tokens past M just cost zero registers.
+//  - A dot product inside one 128-wide block does not depend on the order of
+//    its terms. Each lane therefore loads 16 contiguous bytes of a weight row
+//    straight into its A-fragment registers (no shared-memory staging), and
+//    the activation fragment is loaded with the same K permutation:
+//    lane (g, t) = (lane/4, lane%4) reads bytes [16t, 16t+16) and
+//    [64+16t, 64+16t+16) of the block for weight rows g and g+8 and for token
+//    g; MMA i of the block takes words 2i and 2i+1 of those 32 bytes. Over
+//    t = 0..3 and i = 0..3 every byte of the block is used exactly once.
+//  - Four MMAs (K = 128) accumulate one block's dot in fp32; it is then scaled
+//    by sa[m, kb] * sw[n/128, kb] and added into the warp's running sums.
+//  - The warps' partial sums meet in shared memory and one pass writes the
+//    16 x M outputs (bf16, or fp32 for the error-analysis entry point).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fp8act {
+namespace {
+
+constexpr int kMaxWarps = 16;
+constexpr int kUnroll = 2;  // K blocks whose loads a warp has in flight at once
+
+__device__ __forceinline__ void mma_e4m3_16x8x32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <bool kF32Out>
+__global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
+    const uint8_t* __restrict__ q, const float* __restrict__ sa, const uint8_t* __restrict__ w,
+    const float* __restrict__ sw, int M, int N, int K, void* __restrict__ out) {
+    __shared__ float red[kMaxWarps][16][8];
+
+    const int KB = K / kGroup;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int n0 = blockIdx.x * 16;
+    const int m0 = blockIdx.y * 8;
+    const int mt = min(8, M - m0);
+
+    const bool ok_r0 = n0 + g < N;
+    const bool ok_r1 = n0 + g + 8 < N;
+    const bool ok_x = g < mt;
+    const uint8_t* w_r0 = w + static_cast<int64_t>(n0 + g) * K + 16 * t;
+    const uint8_t* w_r1 = w + static_cast<int64_t>(n0 + g + 8) * K + 16 * t;
+    const uint8_t* x_r = q + static_cast<int64_t>(m0 + g) * K + 16 * t;
+
+    const int c0 = 2 * t, c1 = 2 * t + 1;  // token columns of this lane's accumulators
+    const bool ok_c0 = c0 < mt, ok_c1 = c1 < mt;
+    const float* sa_c0 = sa + static_cast<int64_t>(m0 + c0) * KB;
+    const float* sa_c1 = sa + static_cast<int64_t>(m0 + c1) * KB;
+    const float* sw_r = sw + static_cast<int64_t>(n0 / kGroup) * KB;
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+
+    for (int kb0 = warp; kb0 < KB; kb0 += nwarps * kUnroll) {
+        uint4 r0lo[kUnroll], r0hi[kUnroll], r1lo[kUnroll], r1hi[kUnroll], xlo[kUnroll], xhi[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int kb = kb0 + u * nwarps;
+            const bool ok_k = kb < KB;
+            const int64_t off = static_cast<int64_t>(kb) * kGroup;
+            r0lo[u] = (ok_k && ok_r0) ? ld_stream_v4(w_r0 + off) : zero;
+            r0hi[u] = (ok_k && ok_r0) ? ld_stream_v4(w_r0 + off + 64) : zero;
+            r1lo[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off) : zero;
+            r1hi[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off + 64) : zero;
+            xlo[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off) : zero;
+            xhi[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off + 64) : zero;
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int kb = kb0 + u * nwarps;
+            if (kb < KB) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_e4m3_16x8x32(d, r0lo[u].x, r1lo[u].x, r0lo[u].y, r1lo[u].y, xlo[u].x, xlo[u].y);
+                mma_e4m3_16x8x32(d, r0lo[u].z, r1lo[u].z, r0lo[u].w, r1lo[u].w, xlo[u].z, xlo[u].w);
+                mma_e4m3_16x8x32(d, r0hi[u].x, r1hi[u].x, r0hi[u].y, r1hi[u].y, xhi[u].x, xhi[u].y);
+                mma_e4m3_16x8x32(d, r0hi[u].z, r1hi[u].z, r0hi[u].w, r1hi[u].w, xhi[u].z, xhi[u].w);
+                const float s_w = __ldg(sw_r + kb);
+                const float s0 = ok_c0 ? __ldg(sa_c0 + kb) * s_w : 0.f;
+                const float s1 = ok_c1 ? __ldg(sa_c1 + kb) * s_w : 0.f;
+                acc[0] = fmaf(d[0], s0, acc[0]);
+                acc[1] = fmaf(d[1], s1, acc[1]);
+                acc[2] = fmaf(d[2], s0, acc[2]);
+                acc[3] = fmaf(d[3], s1, acc[3]);
+            }
+        }
+    }
+
+    red[warp][g][c0] = acc[0];
+    red[warp][g][c1] = acc[1];
+    red[warp][g + 8][c0] = acc[2];
+    red[warp][g + 8][c1] = acc[3];
+    __syncthreads();
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        const int r = i & 15;  // consecutive threads write consecutive n
+        const int c = i >> 4;
+        float s = 0.f;
+        for (int ww = 0; ww < nwarps; ++ww) s += red[ww][r][c];
+        const int n = n0 + r;
+        if (n < N && c < mt) {
+            const int64_t o = static_cast<int64_t>(m0 + c) * N + n;
+            if constexpr (kF32Out) {
+                static_cast<float*>(out)[o] = s;
+            } else {
+                static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(s);
+            }
+        }
+    }
+}
+
+// Warps per CTA: the largest divisor of K/128 (<= kMaxWarps) for which the
+// whole grid is resident at once (one wave: every warp has the same number of
+// K blocks, so all of them finish together), else the smallest grid-friendly
+// choice of 4 warps.
+template <bool kF32Out>
+int pick_warps(int64_t ctas, int KB, int num_sms) {
+    for (int wv = kMaxWarps; wv >= 1; --wv) {
+        if (wv > KB || KB % wv) continue;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out>, 32 * wv, 0) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            break;
+        }
+        if (ctas <= static_cast<int64_t>(per_sm) * num_sms) return wv;
+    }
+    return KB < 4 ? KB : 4;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_skinny(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
+                               int N, int K, void* out, bool out_f32, int num_sms, cudaStream_t stream) {
+    const int KB = K / kGroup;
+    const dim3 grid((N + 15) / 16, (M + 7) / 8);
+    const int64_t ctas = static_cast<int64_t>(grid.x) * grid.y;
+    if (out_f32) {
+        const dim3 block(32 * pick_warps<true>(ctas, KB, num_sms));
+        gemm_skinny_kernel<true><<<grid, block, 0, stream>>>(q, sa, w, sw, M, N, K, out);
+    } else {
+        const dim3 block(32 * pick_warps<false>(ctas, KB, num_sms));
+        gemm_skinny_kernel<false><<<grid, block, 0, stream>>>(q, sa, w, sw, M, N, K, out);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace fp8act

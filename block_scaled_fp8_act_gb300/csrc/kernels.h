@@ -1,0 +1,23 @@
+// Host-side launchers of libfp8act's kernels (internal; the public API is include/fp8act.h).
+// Arguments are validated by the C-ABI layer before any of these is called.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8act {
+
+// Activation quantisation, x bf16 [M, K] -> q E4M3 [M, K], sa fp32 [M, K/128].
+cudaError_t launch_act_quant(const void* x, int64_t M, int64_t K, void* q, float* sa, int num_sms,
+                             cudaStream_t stream);
+
+// Weight quantisation, W bf16 [N, K] -> w E4M3 [N, K], sw fp32 [ceil(N/128), K/128].
+cudaError_t launch_weight_quant(const void* W, int64_t N, int64_t K, void* w, float* sw, cudaStream_t stream);
+
+// Weight-streaming GEMM for small M (tensor-core mma.sync, 16-row tiles,
+// K split across the warps of a CTA). Any M works (tokens in groups of 8)
+// but it re-reads the weights once per group, so it is the M <= 16 path.
+cudaError_t launch_gemm_skinny(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
+                               int N, int K, void* out, bool out_f32, int num_sms, cudaStream_t stream);
+
+}  // namespace fp8act

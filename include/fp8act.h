@@ -1,0 +1,118 @@
+/*
+ * fp8act.h - C ABI of libfp8act.so, the W8A8 block-FP8 linear layer for GB300 (sm_103a).
+ *
+ * The layer: y = x W^T with x [M, K] quantised per token in 1x128 K groups and
+ * W [N, K] quantised per 128x128 block, both to FP8 E4M3 with one fp32 scale
+ * per group / block, multiplied with fp32 accumulation and stored as bf16.
+ * "W8A8 Block FP8" is the layer type of the five projection shapes in
+ * "双 NVIDIA L20 上 Qwen3.8-27B-FP8 + MTP 调优测试报告" (ownding.com), section 八
+ * (L20 FP8 kernel tuning). The run-time activation quantisation is the step
+ * that "单并发提速73%,多并发能力达原来2.4倍:Qwen3.8-27B性能优化实践"
+ * (smartx.com), section "单并发优化", credits the weight-only Marlin back-end
+ * with skipping. Neither page fixes the arithmetic; this library implements:
+ *
+ *   s      = amax / 448 over the group (fp32, IEEE division); s = 1 if amax = 0
+ *   code   = E4M3(x / s): IEEE fp32 division, round to nearest even,
+ *            saturated to +-448 (largest finite E4M3), sign of zero kept
+ *   y[m,n] = sum_kb sa[m,kb] * sw[n/128,kb] * sum_{k in block kb} q[m,k] w[n,k]
+ *   out    = bf16(y), round to nearest even
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Pointers are DEVICE pointers on the current CUDA device, owned by the
+ *   caller. The library never allocates, frees or synchronises inside these
+ *   calls and reads no device data on the host, so every call can be
+ *   captured in a CUDA graph.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
+ *   enqueued asynchronously; the returned status covers argument checks and
+ *   the launch only. Kernel-side timeouts are reported by
+ *   fp8act_check_status().
+ * - Layouts are row-major and contiguous: x, q [M, K]; sa [M, K/128];
+ *   W, w [N, K] (K contiguous); sw [ceil(N/128), K/128]; out [M, N].
+ * - K must be a positive multiple of 128. M and N may be any value >= 0; a
+ *   call with M == 0 (or N == 0) does nothing and returns FP8ACT_OK.
+ * - x, q, W, w and out must be 16-byte aligned; sa and sw 4-byte aligned.
+ * - Behaviour on NaN or infinite inputs is unspecified (no error is raised).
+ * - The library runs only on compute capability 10.3 (GB300); on any other
+ *   device every compute call returns FP8ACT_ERR_DEVICE.
+ */
+#ifndef FP8ACT_H
+#define FP8ACT_H
+
+#if defined(__GNUC__)
+#define FP8ACT_API __attribute__((visibility("default")))
+#else
+#define FP8ACT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8ACT_OK = 0,
+    FP8ACT_ERR_NULL = 1,     /* a required pointer is NULL                         */
+    FP8ACT_ERR_SHAPE = 2,    /* M, N < 0; K <= 0 or K % 128 != 0; size overflow   */
+    FP8ACT_ERR_ALIGN = 3,    /* a pointer violates the alignment rule above       */
+    FP8ACT_ERR_LAUNCH = 4,   /* the kernel launch failed (cudaGetLastError)       */
+    FP8ACT_ERR_TIMEOUT = 5,  /* a kernel's bounded wait gave up (see check_status) */
+    FP8ACT_ERR_DEVICE = 6,   /* no current device, or not compute capability 10.3 */
+    FP8ACT_ERR_CUDA = 7      /* another CUDA runtime error                         */
+} fp8act_status;
+
+/*
+ * Activation quantisation, one scale per token and 128-wide K group.
+ *   x_bf16  [M, K] bf16 in
+ *   q_e4m3  [M, K] E4M3 codes out (1 byte each)
+ *   sa      [M, K/128] fp32 scales out
+ * Bit-exact with the definition above.
+ */
+FP8ACT_API int fp8_act_quant(const void* x_bf16, int M, int K, void* q_e4m3, float* sa, void* stream);
+
+/*
+ * Weight quantisation, one scale per 128x128 block (an offline step: the
+ * served checkpoint stores w and sw). A partial block at the N edge takes its
+ * amax over the rows that exist.
+ *   w_bf16  [N, K] bf16 in
+ *   w_e4m3  [N, K] E4M3 codes out
+ *   sw      [ceil(N/128), K/128] fp32 scales out
+ */
+FP8ACT_API int fp8_weight_quant(const void* w_bf16, int N, int K, void* w_e4m3, float* sw, void* stream);
+
+/*
+ * Block-scaled GEMM: out[M, N] = bf16(y) with y as defined above, fp32
+ * accumulation. Dispatches on M: a weight-streaming kernel for M <= 16,
+ * tensor-memory (tcgen05) kernels above. Every M >= 1 is supported.
+ *   q_e4m3, sa : activation codes [M, K] and scales [M, K/128]
+ *   w_e4m3, sw : weight codes [N, K] and scales [ceil(N/128), K/128]
+ *   out_bf16   : [M, N] bf16 out
+ */
+FP8ACT_API int fp8_block_gemm(const void* q_e4m3, const float* sa, const void* w_e4m3, const float* sw,
+                   int M, int N, int K, void* out_bf16, void* stream);
+
+/*
+ * The same kernels as fp8_block_gemm with an fp32 store in place of the
+ * bf16 cast (for error analysis of the accumulation before rounding).
+ */
+FP8ACT_API int fp8_block_gemm_f32(const void* q_e4m3, const float* sa, const void* w_e4m3, const float* sw,
+                       int M, int N, int K, float* out_f32, void* stream);
+
+/* A static English description of a status code (never NULL). */
+FP8ACT_API const char* fp8act_strerror(int status);
+
+/*
+ * Synchronises `stream` and reports whether any kernel of this library on the
+ * current device gave up a bounded wait since the last call (FP8ACT_ERR_TIMEOUT),
+ * then clears the flag. Returns FP8ACT_ERR_CUDA if the stream itself failed.
+ * Not capturable (it synchronises); meant for tests and health checks.
+ */
+FP8ACT_API int fp8act_check_status(void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+FP8ACT_API int fp8act_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8ACT_H */

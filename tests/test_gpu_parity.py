@@ -1,0 +1,178 @@
+"""GPU parity: the CUDA path against the CPU oracle on the same seeded inputs.
+
+Covers, through the C ABI (via the ctypes binding):
+* activation and weight quantisation, bit-exact, on the five projection
+  shapes, every M of the five workloads, edge-case groups and ragged N;
+* the GEMM on the five shapes at M = 1, 2..8, 64, 102 (every output) and
+  4096 (sampled rows), plus ragged shapes that cross tile and scale-block
+  edges, empty problems, determinism, non-default streams, CUDA-graph
+  capture and out-of-bounds write canaries.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp8_act_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = inputs.SHAPES
+_problems: dict = {}
+
+
+@pytest.fixture(scope="module")
+def fp8act():
+    from block_scaled_fp8_act_gb300 import fp8act as mod
+    mod.load(build=True)
+    return mod
+
+
+def problem(si: int):
+    from parity_util import Problem
+    if si not in _problems:
+        N, K = SHAPES[si]
+        _problems[si] = Problem(N, K, inputs.weight_seed(si))
+    return _problems[si]
+
+
+# ------------------------------------------------------------ quantisation
+@pytest.mark.parametrize("K", sorted({k for _, k in SHAPES}))
+@pytest.mark.parametrize("M", [1, 5, 8, 64, 102])
+def test_act_quant_bit_exact(fp8act, M, K):
+    x = inputs.activations_bf16(M, K, seed=3000 + M)
+    q_ref, sa_ref = oracle.act_quant(inputs.bf16_bits(x))
+    q, sa = fp8act.fp8_act_quant(x.cuda())
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(sa.cpu().numpy(), sa_ref)
+
+
+@pytest.mark.parametrize("M,K", [(1, 9 * 128), (7, 5120), (33, 3072)])
+def test_act_quant_edge_groups_bit_exact(fp8act, M, K):
+    x = inputs.edge_activations_bf16(M, K, seed=M)
+    q_ref, sa_ref = oracle.act_quant(inputs.bf16_bits(x))
+    q, sa = fp8act.fp8_act_quant(x.cuda())
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(sa.cpu().numpy(), sa_ref)
+
+
+def test_act_quant_prefill_size_bit_exact(fp8act):
+    x = inputs.activations_bf16(4096, 8704, seed=4096)
+    q_ref, sa_ref = oracle.act_quant(inputs.bf16_bits(x))
+    q, sa = fp8act.fp8_act_quant(x.cuda())
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(sa.cpu().numpy(), sa_ref)
+
+
+@pytest.mark.parametrize("si", range(len(SHAPES)))
+def test_weight_quant_bit_exact_projection_shapes(fp8act, si):
+    p = problem(si)
+    assert np.array_equal(p.w.cpu().numpy(), p.w_ref)
+    assert np.array_equal(p.sw.cpu().numpy(), p.sw_ref)
+
+
+@pytest.mark.parametrize("N,K", [(200, 256), (1000, 384), (1, 128), (129, 1152)])
+def test_weight_quant_bit_exact_ragged(fp8act, N, K):
+    W = inputs.weights_bf16(N, K, seed=N)
+    w_ref, sw_ref = oracle.weight_quant(inputs.bf16_bits(W))
+    w, sw = fp8act.fp8_weight_quant(W.cuda())
+    assert np.array_equal(w.cpu().numpy(), w_ref)
+    assert np.array_equal(sw.cpu().numpy(), sw_ref)
+
+
+# ------------------------------------------------------------------- GEMM
+@pytest.mark.parametrize("si", range(len(SHAPES)))
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_gemm_decode_and_verify_widths(fp8act, si, M):
+    stats = problem(si).run_and_compare(M, inputs.activation_seed(si, M - 1))
+    assert stats["max_ulp"] <= 1 or stats["floor_used"] > 0
+
+
+@pytest.mark.parametrize("si", range(len(SHAPES)))
+@pytest.mark.parametrize("M", [64, 102])
+def test_gemm_batched_decode(fp8act, si, M):
+    problem(si).run_and_compare(M, inputs.activation_seed(si, 8 + (M == 102)))
+
+
+@pytest.mark.parametrize("si", range(len(SHAPES)))
+def test_gemm_prefill_sampled_rows(fp8act, si):
+    from parity_util import sample_rows
+    rows = sample_rows(4096, 24, seed=si)
+    problem(si).run_and_compare(4096, inputs.activation_seed(si, 10), rows=rows)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 17, 128), (3, 200, 256), (8, 1000, 384), (9, 130, 512),
+                                   (16, 4096, 1024), (63, 300, 640), (65, 257, 768),
+                                   (127, 129, 256), (129, 520, 1152), (300, 384, 384)])
+def test_gemm_ragged_shapes(fp8act, M, N, K):
+    from parity_util import Problem
+    p = Problem(N, K, seed=N + K)
+    p.run_and_compare(M, seed=M + 7)
+
+
+def test_gemm_edge_activations(fp8act):
+    from parity_util import Problem
+    p = Problem(640, 9 * 128, seed=5)
+    for M in (1, 8, 20):
+        p.run_and_compare(M, seed=M, edge=True)
+
+
+def test_gemm_empty_problems(fp8act):
+    q = torch.empty((0, 256), dtype=torch.uint8, device="cuda")
+    sa = torch.empty((0, 2), dtype=torch.float32, device="cuda")
+    w = torch.zeros((128, 256), dtype=torch.uint8, device="cuda")
+    sw = torch.ones((1, 2), dtype=torch.float32, device="cuda")
+    assert fp8act.fp8_block_gemm(q, sa, w, sw).shape == (0, 128)
+
+
+def test_gemm_deterministic_and_stream_safe(fp8act):
+    p = problem(1)
+    q, sa, _, _ = p.activations(8, seed=1)
+    a = fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        b = fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_quant_and_gemm_capture_in_cuda_graph(fp8act):
+    p = problem(1)
+    x = inputs.activations_bf16(4, p.K, seed=9).cuda()
+    q = torch.empty((4, p.K), dtype=torch.uint8, device="cuda")
+    sa = torch.empty((4, p.K // 128), dtype=torch.float32, device="cuda")
+    out = torch.empty((4, p.N), dtype=torch.bfloat16, device="cuda")
+    fp8act.fp8_act_quant(x, q, sa)
+    fp8act.fp8_block_gemm(q, sa, p.w, p.sw, out)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fp8act.fp8_act_quant(x, q, sa, stream=s)
+            fp8act.fp8_block_gemm(q, sa, p.w, p.sw, out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+
+
+def test_gemm_writes_nothing_outside_out(fp8act):
+    p = problem(1)
+    for M in (1, 7, 70):
+        q, sa, _, _ = p.activations(M, seed=M)
+        pad = 4096
+        buf = torch.full((M * p.N + 2 * pad,), -7.0, dtype=torch.bfloat16, device="cuda")
+        out = buf[pad:pad + M * p.N].view(M, p.N)
+        fp8act.fp8_block_gemm(q, sa, p.w, p.sw, out)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:pad] == -7.0) and torch.all(buf[pad + M * p.N:] == -7.0)
+
+
+def test_status_is_clean(fp8act):
+    assert fp8act.check_status() == 0
