@@ -73,11 +73,16 @@ def load_peaks() -> tuple[dict, str]:
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Short hash of the CUDA sources, to tell whether recorded ncu traffic is current."""
+KERNEL_SOURCES = {
+    "gemm_skinny_kernel": ("gemm_skinny.cu", "common.cuh", "sm100_ptx.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Short hash of a kernel's CUDA sources, to tell whether recorded ncu traffic is current."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_fp8_act_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -89,7 +94,7 @@ def recorded_traffic(kernel: str, workload: str) -> float | None:
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     for line in open(path, encoding="utf-8"):
         parts = line.split()
         if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload \
@@ -356,6 +361,7 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work to time")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -410,7 +416,7 @@ def main() -> None:
         wl.enqueue_step(c, stream)
         for si in range(len(wl.shapes)):
             wl.out_host[si].copy_(wl.out[si], non_blocking=True)
-    e2e_steps = max(50, args.steps // 10)
+    e2e_steps = 0 if args.no_e2e else max(50, args.steps // 10)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             e2e_step(i % wl.copies)
@@ -422,8 +428,8 @@ def main() -> None:
             e2e_step(i % wl.copies)
         s1.record(stream)
         s1.synchronize()
-        wall = (time.perf_counter() - t0) / e2e_steps
-    t_e2e = max(s0.elapsed_time(s1) / 1e3 / e2e_steps, wall)
+        wall = (time.perf_counter() - t0) / max(e2e_steps, 1)
+    t_e2e = max(s0.elapsed_time(s1) / 1e3 / max(e2e_steps, 1), wall)
     t_e2e = max_over_ranks(world, t_e2e)
     h2d = sum(x.numel() * 2 for x in wl.x_host)
     d2h = sum(o.numel() * 2 for o in wl.out_host)

@@ -60,9 +60,9 @@ int gemm_common(const void* q, const float* sa, const void* w, const float* sw, 
     const int sms = current_device_sms(&st);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_status(fp8act::launch_gemm_skinny(static_cast<const uint8_t*>(q), sa,
-                                                    static_cast<const uint8_t*>(w), sw, M, N, K, out, out_f32,
-                                                    sms, s));
+    const uint8_t* q8 = static_cast<const uint8_t*>(q);
+    const uint8_t* w8 = static_cast<const uint8_t*>(w);
+    return launch_status(fp8act::launch_gemm_skinny(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
 }
 
 }  // namespace

@@ -33,14 +33,16 @@
 //    by sa[m, kb] * sw[n/128, kb] and added into the warp's running sums.
 //  - The warps' partial sums meet in shared memory and one pass writes the
 //    16 x M outputs (bf16, or fp32 for the error-analysis entry point).
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100_ptx.cuh"
 
 namespace fp8act {
 namespace {
 
 constexpr int kMaxWarps = 16;
-constexpr int kUnroll = 2;  // K blocks whose loads a warp has in flight at once
 
 __device__ __forceinline__ void mma_e4m3_16x8x32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                   uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -51,11 +53,13 @@ __device__ __forceinline__ void mma_e4m3_16x8x32(float (&d)[4], uint32_t a0, uin
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <bool kF32Out>
+// kUnroll = K blocks whose weight loads a warp has in flight at once;
+// kTG = groups of 8 tokens a CTA handles (they share the weight fragments).
+template <bool kF32Out, int kUnroll, int kTG>
 __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
     const uint8_t* __restrict__ q, const float* __restrict__ sa, const uint8_t* __restrict__ w,
     const float* __restrict__ sw, int M, int N, int K, void* __restrict__ out) {
-    __shared__ float red[kMaxWarps][16][8];
+    __shared__ float red[kMaxWarps][16][8 * kTG];
 
     const int KB = K / kGroup;
     const int lane = threadIdx.x & 31;
@@ -64,27 +68,26 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
     const int g = lane >> 2;
     const int t = lane & 3;
     const int n0 = blockIdx.x * 16;
-    const int m0 = blockIdx.y * 8;
-    const int mt = min(8, M - m0);
+    const int m0 = blockIdx.y * 8 * kTG;
 
     const bool ok_r0 = n0 + g < N;
     const bool ok_r1 = n0 + g + 8 < N;
-    const bool ok_x = g < mt;
     const uint8_t* w_r0 = w + static_cast<int64_t>(n0 + g) * K + 16 * t;
     const uint8_t* w_r1 = w + static_cast<int64_t>(n0 + g + 8) * K + 16 * t;
-    const uint8_t* x_r = q + static_cast<int64_t>(m0 + g) * K + 16 * t;
-
-    const int c0 = 2 * t, c1 = 2 * t + 1;  // token columns of this lane's accumulators
-    const bool ok_c0 = c0 < mt, ok_c1 = c1 < mt;
-    const float* sa_c0 = sa + static_cast<int64_t>(m0 + c0) * KB;
-    const float* sa_c1 = sa + static_cast<int64_t>(m0 + c1) * KB;
     const float* sw_r = sw + static_cast<int64_t>(n0 / kGroup) * KB;
 
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[kTG][4];
+#pragma unroll
+    for (int j = 0; j < kTG; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
     const uint4 zero = make_uint4(0, 0, 0, 0);
 
+    // Programmatic dependent launch: the weights never depend on the previous
+    // grid, so the first weight loads go out before waiting for it; the
+    // activations, scales and output are touched only after the wait.
+    ptx::griddep_launch_dependents();
+    bool waited = false;
     for (int kb0 = warp; kb0 < KB; kb0 += nwarps * kUnroll) {
-        uint4 r0lo[kUnroll], r0hi[kUnroll], r1lo[kUnroll], r1hi[kUnroll], xlo[kUnroll], xhi[kUnroll];
+        uint4 r0lo[kUnroll], r0hi[kUnroll], r1lo[kUnroll], r1hi[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int kb = kb0 + u * nwarps;
@@ -94,46 +97,68 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
             r0hi[u] = (ok_k && ok_r0) ? ld_stream_v4(w_r0 + off + 64) : zero;
             r1lo[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off) : zero;
             r1hi[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off + 64) : zero;
-            xlo[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off) : zero;
-            xhi[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off + 64) : zero;
+        }
+        if (!waited) {
+            ptx::griddep_wait();
+            waited = true;
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int kb = kb0 + u * nwarps;
-            if (kb < KB) {
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_e4m3_16x8x32(d, r0lo[u].x, r1lo[u].x, r0lo[u].y, r1lo[u].y, xlo[u].x, xlo[u].y);
-                mma_e4m3_16x8x32(d, r0lo[u].z, r1lo[u].z, r0lo[u].w, r1lo[u].w, xlo[u].z, xlo[u].w);
-                mma_e4m3_16x8x32(d, r0hi[u].x, r1hi[u].x, r0hi[u].y, r1hi[u].y, xhi[u].x, xhi[u].y);
-                mma_e4m3_16x8x32(d, r0hi[u].z, r1hi[u].z, r0hi[u].w, r1hi[u].w, xhi[u].z, xhi[u].w);
-                const float s_w = __ldg(sw_r + kb);
-                const float s0 = ok_c0 ? __ldg(sa_c0 + kb) * s_w : 0.f;
-                const float s1 = ok_c1 ? __ldg(sa_c1 + kb) * s_w : 0.f;
-                acc[0] = fmaf(d[0], s0, acc[0]);
-                acc[1] = fmaf(d[1], s1, acc[1]);
-                acc[2] = fmaf(d[2], s0, acc[2]);
-                acc[3] = fmaf(d[3], s1, acc[3]);
+        for (int j = 0; j < kTG; ++j) {
+            const int m = m0 + 8 * j + g;  // this lane's token for the B fragment
+            const bool ok_x = m < M;
+            const uint8_t* x_r = q + static_cast<int64_t>(m) * K + 16 * t;
+            const int c0 = m0 + 8 * j + 2 * t;  // token columns of this lane's accumulators
+            uint4 xlo[kUnroll], xhi[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int kb = kb0 + u * nwarps;
+                const bool ok_k = kb < KB;
+                const int64_t off = static_cast<int64_t>(kb) * kGroup;
+                xlo[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off) : zero;
+                xhi[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off + 64) : zero;
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int kb = kb0 + u * nwarps;
+                if (kb < KB) {
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_e4m3_16x8x32(d, r0lo[u].x, r1lo[u].x, r0lo[u].y, r1lo[u].y, xlo[u].x, xlo[u].y);
+                    mma_e4m3_16x8x32(d, r0lo[u].z, r1lo[u].z, r0lo[u].w, r1lo[u].w, xlo[u].z, xlo[u].w);
+                    mma_e4m3_16x8x32(d, r0hi[u].x, r1hi[u].x, r0hi[u].y, r1hi[u].y, xhi[u].x, xhi[u].y);
+                    mma_e4m3_16x8x32(d, r0hi[u].z, r1hi[u].z, r0hi[u].w, r1hi[u].w, xhi[u].z, xhi[u].w);
+                    const float s_w = __ldg(sw_r + kb);
+                    const float s0 = c0 < M ? __ldg(sa + static_cast<int64_t>(c0) * KB + kb) * s_w : 0.f;
+                    const float s1 = c0 + 1 < M ? __ldg(sa + static_cast<int64_t>(c0 + 1) * KB + kb) * s_w : 0.f;
+                    acc[j][0] = fmaf(d[0], s0, acc[j][0]);
+                    acc[j][1] = fmaf(d[1], s1, acc[j][1]);
+                    acc[j][2] = fmaf(d[2], s0, acc[j][2]);
+                    acc[j][3] = fmaf(d[3], s1, acc[j][3]);
+                }
             }
         }
     }
+    if (!waited) ptx::griddep_wait();
 
-    red[warp][g][c0] = acc[0];
-    red[warp][g][c1] = acc[1];
-    red[warp][g + 8][c0] = acc[2];
-    red[warp][g + 8][c1] = acc[3];
+#pragma unroll
+    for (int j = 0; j < kTG; ++j) {
+        red[warp][g][8 * j + 2 * t] = acc[j][0];
+        red[warp][g][8 * j + 2 * t + 1] = acc[j][1];
+        red[warp][g + 8][8 * j + 2 * t] = acc[j][2];
+        red[warp][g + 8][8 * j + 2 * t + 1] = acc[j][3];
+    }
     __syncthreads();
-    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+    for (int i = threadIdx.x; i < 16 * 8 * kTG; i += blockDim.x) {
         const int r = i & 15;  // consecutive threads write consecutive n
         const int c = i >> 4;
-        float s = 0.f;
-        for (int ww = 0; ww < nwarps; ++ww) s += red[ww][r][c];
+        float v = 0.f;
+        for (int ww = 0; ww < nwarps; ++ww) v += red[ww][r][c];
         const int n = n0 + r;
-        if (n < N && c < mt) {
+        if (n < N && m0 + c < M) {
             const int64_t o = static_cast<int64_t>(m0 + c) * N + n;
             if constexpr (kF32Out) {
-                static_cast<float*>(out)[o] = s;
+                static_cast<float*>(out)[o] = v;
             } else {
-                static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(s);
+                static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(v);
             }
         }
     }
@@ -142,37 +167,77 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
 // Warps per CTA: the largest divisor of K/128 (<= kMaxWarps) for which the
 // whole grid is resident at once (one wave: every warp has the same number of
 // K blocks, so all of them finish together), else the smallest grid-friendly
-// choice of 4 warps.
-template <bool kF32Out>
+// choice of 4 warps. Occupancy answers are cached per (device, warps).
+template <bool kF32Out, int kUnroll, int kTG>
 int pick_warps(int64_t ctas, int KB, int num_sms) {
+    static std::atomic<int> per_sm_cache[64][kMaxWarps + 1];  // 0 = unknown, else 1 + CTAs per SM
+    int dev = 0;
+    cudaGetDevice(&dev);
     for (int wv = kMaxWarps; wv >= 1; --wv) {
         if (wv > KB || KB % wv) continue;
-        int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out>, 32 * wv, 0) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            break;
+        int cached = per_sm_cache[dev & 63][wv].load(std::memory_order_relaxed);
+        if (cached == 0) {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out, kUnroll, kTG>, 32 * wv,
+                                                              0) != cudaSuccess) {
+                cudaGetLastError();
+                break;
+            }
+            cached = per_sm + 1;
+            per_sm_cache[dev & 63][wv].store(cached, std::memory_order_relaxed);
         }
-        if (ctas <= static_cast<int64_t>(per_sm) * num_sms) return wv;
+        if (ctas <= static_cast<int64_t>(cached - 1) * num_sms) return wv;
     }
     return KB < 4 ? KB : 4;
 }
 
+template <bool kF32Out, int kUnroll, int kTG>
+cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N, int K,
+                         void* out, int num_sms, cudaStream_t stream) {
+    const int KB = K / kGroup;
+    const dim3 grid((N + 15) / 16, (M + 8 * kTG - 1) / (8 * kTG));
+    const int64_t ctas = static_cast<int64_t>(grid.x) * grid.y;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(32 * pick_warps<kF32Out, kUnroll, kTG>(ctas, KB, num_sms));
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<kF32Out, kUnroll, kTG>, q, sa, w, sw, M, N, K, out);
+}
+
 }  // namespace
+
+cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
+                                      int N, int K, void* out, bool out_f32, int num_sms, int unroll,
+                                      cudaStream_t stream) {
+    if (M > 8)  // two token groups per CTA: the weight fragments serve 16 tokens
+        return out_f32 ? launch_typed<true, 2, 2>(q, sa, w, sw, M, N, K, out, num_sms, stream)
+                       : launch_typed<false, 2, 2>(q, sa, w, sw, M, N, K, out, num_sms, stream);
+    if (unroll >= 4)
+        return out_f32 ? launch_typed<true, 4, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream)
+                       : launch_typed<false, 4, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream);
+    return out_f32 ? launch_typed<true, 2, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream)
+                   : launch_typed<false, 2, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream);
+}
 
 cudaError_t launch_gemm_skinny(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
                                int N, int K, void* out, bool out_f32, int num_sms, cudaStream_t stream) {
-    const int KB = K / kGroup;
-    const dim3 grid((N + 15) / 16, (M + 7) / 8);
-    const int64_t ctas = static_cast<int64_t>(grid.x) * grid.y;
-    if (out_f32) {
-        const dim3 block(32 * pick_warps<true>(ctas, KB, num_sms));
-        gemm_skinny_kernel<true><<<grid, block, 0, stream>>>(q, sa, w, sw, M, N, K, out);
-    } else {
-        const dim3 block(32 * pick_warps<false>(ctas, KB, num_sms));
-        gemm_skinny_kernel<false><<<grid, block, 0, stream>>>(q, sa, w, sw, M, N, K, out);
+    // Load depth: a warp that streams >= 8 K blocks keeps 4 of them in flight
+    // (fewer warps fit, but each covers more of the latency); shorter K
+    // ranges keep 2 and more warps. The warp count comes from the depth-2
+    // configuration's single-wave rule.
+    int unroll = 2;
+    if (M <= 8) {
+        const int KB = K / kGroup;
+        const int64_t ctas = (N + 15) / 16;
+        const int wv = out_f32 ? pick_warps<true, 2, 1>(ctas, KB, num_sms) : pick_warps<false, 2, 1>(ctas, KB, num_sms);
+        if (KB / wv >= 8) unroll = 4;
     }
-    return cudaGetLastError();
+    return launch_gemm_skinny_unroll(q, sa, w, sw, M, N, K, out, out_f32, num_sms, unroll, stream);
 }
 
 }  // namespace fp8act

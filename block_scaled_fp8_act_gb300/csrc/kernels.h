@@ -15,9 +15,14 @@ cudaError_t launch_act_quant(const void* x, int64_t M, int64_t K, void* q, float
 cudaError_t launch_weight_quant(const void* W, int64_t N, int64_t K, void* w, float* sw, cudaStream_t stream);
 
 // Weight-streaming GEMM for small M (tensor-core mma.sync, 16-row tiles,
-// K split across the warps of a CTA). Any M works (tokens in groups of 8)
-// but it re-reads the weights once per group, so it is the M <= 16 path.
+// K split across the warps of a CTA, programmatic dependent launch). Any M
+// works (tokens in groups of 16 above M = 8) but it re-reads the weights
+// once per group, so it is the M <= 16 path.
 cudaError_t launch_gemm_skinny(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
                                int N, int K, void* out, bool out_f32, int num_sms, cudaStream_t stream);
+// The same with an explicit load depth per warp (2 or 4 K blocks in flight).
+cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
+                                      int N, int K, void* out, bool out_f32, int num_sms, int unroll,
+                                      cudaStream_t stream);
 
 }  // namespace fp8act

@@ -10,6 +10,7 @@
 // fp32 scale.
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100_ptx.cuh"
 
 namespace fp8act {
 namespace {
@@ -30,6 +31,11 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict_
     const int64_t nwarp = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t per_iter = 2 * kActUnroll;  // groups one warp handles per iteration
 
+    // Programmatic dependent launch: let the next kernel (the GEMM, whose
+    // weight stream does not depend on us) start launching now, then wait for
+    // the grid that produced x (and may still read q / sa) to finish.
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
     for (int64_t base = warp * per_iter; base < groups; base += nwarp * per_iter) {
         uint4 v[kActUnroll];
 #pragma unroll
@@ -116,9 +122,17 @@ cudaError_t launch_act_quant(const void* x, int64_t M, int64_t K, void* q, float
     int64_t blocks = (groups + groups_per_block - 1) / groups_per_block;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    act_quant_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4*>(x), groups, static_cast<uint2*>(q), sa);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, act_quant_kernel, static_cast<const uint4*>(x), groups,
+                              static_cast<uint2*>(q), sa);
 }
 
 cudaError_t launch_weight_quant(const void* W, int64_t N, int64_t K, void* w, float* sw, cudaStream_t stream) {

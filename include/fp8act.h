@@ -81,8 +81,12 @@ FP8ACT_API int fp8_weight_quant(const void* w_bf16, int N, int K, void* w_e4m3, 
 
 /*
  * Block-scaled GEMM: out[M, N] = bf16(y) with y as defined above, fp32
- * accumulation. Dispatches on M: a weight-streaming kernel for M <= 16,
- * tensor-memory (tcgen05) kernels above. Every M >= 1 is supported.
+ * accumulation. Dispatches on M: for M <= 16 a weight-streaming kernel over
+ * 16-row weight tiles (each tile's whole K on one SM, summed in a fixed
+ * order, so results are bit-reproducible); larger M take tile kernels.
+ * Every M >= 1 is supported. Kernels launch with programmatic dependent
+ * launch: the weight stream starts before the previous kernel on the stream
+ * has finished, and activations are read only after it has.
  *   q_e4m3, sa : activation codes [M, K] and scales [M, K/128]
  *   w_e4m3, sw : weight codes [N, K] and scales [ceil(N/128), K/128]
  *   out_bf16   : [M, N] bf16 out

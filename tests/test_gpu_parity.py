@@ -162,9 +162,15 @@ def test_quant_and_gemm_capture_in_cuda_graph(fp8act):
     assert torch.equal(out, eager)
 
 
+@pytest.mark.parametrize("si", [0, 1, 2])
+@pytest.mark.parametrize("M", [9, 12, 16])
+def test_gemm_verify_widths_up_to_16(fp8act, si, M):
+    problem(si).run_and_compare(M, inputs.activation_seed(si, 11 + M))
+
+
 def test_gemm_writes_nothing_outside_out(fp8act):
     p = problem(1)
-    for M in (1, 7, 70):
+    for M in (1, 7, 13, 70):
         q, sa, _, _ = p.activations(M, seed=M)
         pad = 4096
         buf = torch.full((M * p.N + 2 * pad,), -7.0, dtype=torch.bfloat16, device="cuda")
