@@ -22,6 +22,12 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Two fp32 values rounded to bf16 (nearest even) and packed as (lo | hi << 16).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // 16-byte load of data read exactly once: read-only path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 v;

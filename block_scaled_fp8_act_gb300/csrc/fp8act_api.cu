@@ -11,6 +11,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kGroup = 128;
+constexpr int kSkinnyMaxM = 16;  // M up to this streams weights through mma.sync; above, tcgen05 tiles
 
 // Per-device facts looked up once: -1 = unknown, 0 = unsupported, else SM count.
 std::atomic<int> g_device_sms[kMaxDevices];
@@ -62,7 +63,9 @@ int gemm_common(const void* q, const float* sa, const void* w, const float* sw, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint8_t* q8 = static_cast<const uint8_t*>(q);
     const uint8_t* w8 = static_cast<const uint8_t*>(w);
-    return launch_status(fp8act::launch_gemm_skinny(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
+    if (M <= kSkinnyMaxM)
+        return launch_status(fp8act::launch_gemm_skinny(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
+    return launch_status(fp8act::launch_gemm_tc(q8, sa, w8, sw, M, N, K, out, out_f32, s));
 }
 
 }  // namespace
@@ -122,6 +125,7 @@ int fp8act_check_status(void* stream) {
         cudaGetLastError();
         return FP8ACT_ERR_CUDA;
     }
+    if (fp8act::read_and_clear_tc_error()) return FP8ACT_ERR_TIMEOUT;
     return FP8ACT_OK;
 }
 
