@@ -44,7 +44,21 @@ from block_scaled_fp8_act_gb300 import inputs  # noqa: E402
 
 G = 128
 METRIC = "us/call and achieved HBM GB/s (% of roofline) for block-FP8 GEMM at M=1-8"
-WORKLOAD = "decode M=1 over the five dense-27B projection shapes (act quant + block-FP8 GEMM per shape)"
+WORKLOADS = {
+    # name: (M, description, roofline bound)
+    "decode": (1, "decode M=1 over the five dense-27B projection shapes (act quant + block-FP8 GEMM per shape)",
+               "hbm"),
+    "verify": (8, "speculative verify M={M} (draft k={k}) over the five dense-27B projection shapes "
+                  "(act quant + block-FP8 GEMM per shape)", "hbm"),
+    "batched": (102, "batched decode M={M} over the five dense-27B projection shapes "
+                     "(act quant + block-FP8 GEMM per shape)", "hbm"),
+    "prefill": (4096, "prefill chunk M={M} over the five dense-27B projection shapes "
+                      "(act quant + block-FP8 GEMM per shape)", "tensor"),
+}
+
+
+def gemm_kernel_name(M: int) -> str:
+    return "gemm_skinny_kernel" if M <= 16 else "gemm_tc_kernel"
 WEIGHT_COPIES = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
@@ -75,6 +89,7 @@ def load_peaks() -> tuple[dict, str]:
 
 KERNEL_SOURCES = {
     "gemm_skinny_kernel": ("gemm_skinny.cu", "common.cuh", "sm100_ptx.cuh"),
+    "gemm_tc_kernel": ("gemm_tc.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
 }
 
 
@@ -321,7 +336,7 @@ def run_reference(args, world: int, rank: int) -> None:
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus,
             "steps": cb["steps_timed"], "warmup": 0, "ms_per_step": cb["seconds_per_step"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "M": 1, "shapes": inputs.SHAPES},
+            "data": "synthetic", "config": {"workload": WORKLOADS["decode"][1], "M": 1, "shapes": inputs.SHAPES},
             "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
             "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -363,6 +378,9 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work to time")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode",
+                    help="decode (M=1, the headline), verify, batched or prefill")
+    ap.add_argument("--m", type=int, default=None, help="token count for the chosen workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -381,8 +399,13 @@ def main() -> None:
     peaks, peaks_kind = load_peaks()
     stream = torch.cuda.Stream()
 
+    M = args.m if args.m else WORKLOADS[args.workload][0]
+    desc = WORKLOADS[args.workload][1].format(M=M, k=M - 1)
+    # FP8 ridge point ~560 flop/B (measured tensor / HBM peaks) ~ M = 280 tokens
+    bound = "tensor" if M > 280 else "hbm"
+    kernel = gemm_kernel_name(M)
     weights = Weights(device)
-    wl = Workload(1, weights, device)
+    wl = Workload(M, weights, device)
     graphs = [capture(lambda c=c: wl.enqueue_step(c, stream), stream) for c in range(wl.copies)]
     launches_per_step = 2 * len(wl.shapes)
 
@@ -404,10 +427,14 @@ def main() -> None:
         barrier(world)
         t_step = start.elapsed_time(end) / 1e3 / args.steps
         # dominant kernel: the block GEMM, timed per shape on the same stream
-        gemm_ts = gemm_kernel_times(wl, stream)
+        gemm_ts = gemm_kernel_times(wl, stream, launches=60 if M <= 128 else 8)
     t_step = max_over_ranks(world, t_step)
     step_bytes = wl.step_bytes()
-    value = world * step_bytes / t_step / 1e9
+    step_flops = sum(2.0 * M * N * K for N, K in wl.shapes)
+    if bound == "tensor":
+        value, unit = world * step_flops / t_step / 1e12, "TFLOP/s"
+    else:
+        value, unit = world * step_bytes / t_step / 1e9, "GB/s"
 
     # ---- e2e: public API, activations from pinned host, outputs back, every step
     def e2e_step(c):
@@ -434,33 +461,46 @@ def main() -> None:
     h2d = sum(x.numel() * 2 for x in wl.x_host)
     d2h = sum(o.numel() * 2 for o in wl.out_host)
 
-    gemm_bytes = [algorithmic_gemm_bytes(1, N, K) for N, K in wl.shapes]
-    achieved = sum(gemm_bytes) / sum(gemm_ts) / 1e9
-    peak = float(peaks["hbm_gbs"])
-    traffic = recorded_traffic("gemm_skinny_kernel", "decode_m1_mean_of_5")
-    per_shape = [{"N": N, "K": K, "us_per_call": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1),
-                  "frac": round(b / t / 1e9 / peak, 4)}
-                 for (N, K), t, b in zip(wl.shapes, gemm_ts, gemm_bytes)]
+    gemm_bytes = [algorithmic_gemm_bytes(M, N, K) for N, K in wl.shapes]
+    gemm_flops = [2.0 * M * N * K for N, K in wl.shapes]
+    traffic = recorded_traffic(kernel, f"{args.workload}_m{M}_mean_of_5")
+    if bound == "tensor":
+        achieved = sum(gemm_flops) / sum(gemm_ts) / 1e12
+        peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
+        peak_kind = (f"{peaks_kind} bf16 dense (cuBLAS, burst) x {FP8_OVER_BF16:g}, the nominal FP8/bf16 ratio")
+        roof_unit, per_launch = "TFLOP/s", {"flops_per_launch": sum(gemm_flops) / len(gemm_flops)}
+        per_shape = [{"N": N, "K": K, "us_per_call": round(t * 1e6, 3), "tflops": round(f / t / 1e12, 1),
+                      "frac": round(f / t / 1e12 / peak, 4)}
+                     for (N, K), t, f in zip(wl.shapes, gemm_ts, gemm_flops)]
+    else:
+        achieved = sum(gemm_bytes) / sum(gemm_ts) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        peak_kind = f"{peaks_kind} HBM copy bandwidth"
+        roof_unit, per_launch = "GB/s", {"bytes_per_launch": sum(gemm_bytes) / len(gemm_bytes)}
+        per_shape = [{"N": N, "K": K, "us_per_call": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1),
+                      "frac": round(b / t / 1e9 / peak, 4)}
+                     for (N, K), t, b in zip(wl.shapes, gemm_ts, gemm_bytes)]
 
     del graphs
     torch.cuda.synchronize()
     result = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if args.workload == "decode" else f"block-FP8 linear, {desc}",
+        "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 acc -> bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 1, "shapes": [list(s) for s in wl.shapes],
+        "config": {"workload": desc, "M": M, "shapes": [list(s) for s in wl.shapes],
                    "l2": f"inputs larger than L2: {wl.copies} rotating weight copies "
                          f"({wl.copies * sum(N * K for N, K in wl.shapes) / 1e6:.0f} MB), no flush",
                    "graphs": "each step is one CUDA graph replay (10 kernels)",
                    "parallelism": f"replicas x{world}"},
         "us_per_call": per_shape,
         "gpu_launches": args.steps * launches_per_step,
-        "roofline": {"bound": "hbm", "kernel": "gemm_skinny_kernel", "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "peak_kind": f"{peaks_kind} HBM copy bandwidth",
-                     "bytes_per_launch": sum(gemm_bytes) / len(gemm_bytes),
+        "roofline": {"bound": bound, "kernel": kernel, "achieved": round(achieved, 1),
+                     "peak": round(peak, 1), "unit": roof_unit, "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_kind": peak_kind, **per_launch,
                      "us_per_launch": round(sum(gemm_ts) / len(gemm_ts) * 1e6, 3)},
-        "e2e": {"value": round(world * step_bytes / t_e2e / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(world * (step_flops / 1e12 if bound == "tensor" else step_bytes / 1e9) / t_e2e, 2),
+                "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 5)},
         "clocks": clk.summary(),
     }
