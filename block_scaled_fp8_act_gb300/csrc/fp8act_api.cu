@@ -65,7 +65,7 @@ int gemm_common(const void* q, const float* sa, const void* w, const float* sw, 
     const uint8_t* w8 = static_cast<const uint8_t*>(w);
     if (M <= kSkinnyMaxM)
         return launch_status(fp8act::launch_gemm_skinny(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
-    return launch_status(fp8act::launch_gemm_tc(q8, sa, w8, sw, M, N, K, out, out_f32, s));
+    return launch_status(fp8act::launch_gemm_tc(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
 }
 
 }  // namespace

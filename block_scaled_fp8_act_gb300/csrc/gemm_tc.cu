@@ -5,31 +5,43 @@
 // ridge point, so the kernel is built around the 5th-generation tensor cores.
 // The pages saw exactly this shape regress when served by a kernel tuned for
 // M = 1 ("双 NVIDIA L20 上 Qwen3.8-27B-FP8 + MTP 调优测试报告", sections 五 and 八):
-// prefill gets its own tile kernel.
+// batched decode and prefill get their own tile kernel.
 //
-// One CTA computes a 128 x 256 output tile (128 tokens x 256 weight rows):
-//  * warp 0, one thread: TMA producer. A 4-stage ring of shared-memory
-//    stages, each one 128-wide K group: the 128 x 128 activation tile and the
-//    256 x 128 weight tile, both in the 128-byte swizzled K-major layout. The
-//    weight copies of the first stages go out before the kernel waits on the
+// A CTA computes 128 x BN output tiles (128 tokens x BN weight rows). Without
+// split K the grid is persistent (at most one CTA per SM) and each CTA walks
+// tiles blockIdx.x, blockIdx.x + gridDim.x, ... in m-fastest order (a wave
+// shares its weight tiles through L2); the stage ring and the two TMEM
+// accumulators run on across tile boundaries, so one tile's store overlaps the
+// next tile's first MMAs. Per CTA:
+//  * warp 0, one thread: TMA producer. A ring of shared-memory stages, each
+//    one 128-wide K group: the 128 x 128 activation tile and the BN x 128
+//    weight tile, both in the 128-byte swizzled K-major layout. The weight
+//    copies of the first stages go out before the kernel waits on the
 //    previous grid (programmatic dependent launch).
-//  * warp 1: allocates 512 TMEM columns (two 128 x 256 fp32 accumulators);
+//  * warp 1: allocates 2 BN TMEM columns (two 128 x BN fp32 accumulators);
 //    one thread issues, per K group, four tcgen05.mma kind::f8f6f4
-//    (M = 128, N = 256, K = 32) into one accumulator, then commits to the
+//    (M = 128, N = BN, K = 32) into one accumulator, then commits to the
 //    stage's "empty" barrier (frees the smem) and the accumulator's "full"
 //    barrier.
 //  * warps 2..9: epilogue. The block scales change every 128-wide K group,
 //    so each group's tensor-core result is promoted to a register
-//    accumulator: tcgen05.ld the 128 x 256 fp32 block, multiply by
-//    sa[m, kb] * sw[n / 128, kb] (one value per row and column half) and add,
-//    while the MMA warp fills the other TMEM accumulator. Warp w reads TMEM
-//    lanes 32 (w % 4) .. 32 (w % 4) + 31; warps 2..5 take columns 0..127 and
-//    warps 6..9 columns 128..255, so each thread owns one output row segment
-//    of 128 columns. After the last K group the registers are rounded to
-//    bf16 (or kept fp32) and stored.
-// Every wait is bounded; a timeout sets the error word read by
-// fp8act_check_status() and the kernel runs to completion on whatever data
-// it has (never a hang).
+//    accumulator: tcgen05.ld the group's fp32 block, multiply by
+//    sa[m, kb] * sw[n / 128, kb] and add, while the MMA warp fills the other
+//    TMEM accumulator. Warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31;
+//    warps 2..5 take the first BN / 2 columns and warps 6..9 the rest, so
+//    each thread owns one output row segment of BN / 2 columns.
+//
+// Split K: when the output tiles alone cannot fill the SMs (batched decode on
+// N = 5120 projections has 40 tiles of 128 rows), a cluster of S CTAs shares
+// a tile, each taking a contiguous slice of the K groups. At the end every CTA
+// parks its fp32 partial tile in its own (now idle) stage memory, the cluster
+// synchronises once, and CTA r adds rows [128 r / S, 128 (r + 1) / S) of all S
+// partials through distributed shared memory, in rank order (deterministic),
+// and stores them. No global scratch, no atomics.
+//
+// Every mbarrier wait is bounded; a timeout sets the error word read by
+// fp8act_check_status() and the kernel runs to completion on whatever data it
+// has (never a hang). TMEM is always freed.
 #include <atomic>
 
 #include "common.cuh"
@@ -45,15 +57,22 @@ __device__ unsigned int g_tc_error = 0;
 namespace {
 
 constexpr int BM = 128;  // tokens per tile (TMEM lanes)
-constexpr int BN = 256;  // weight rows per tile (TMEM columns per accumulator)
-constexpr int kStages = 4;
 constexpr int kABytes = BM * kGroup;  // 16 KB
-constexpr int kBBytes = BN * kGroup;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
+
+template <int BN>
+struct TcCfg {
+    static constexpr int kBBytes = BN * kGroup;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = BN == 256 ? 4 : 6;    // ~192 KB of stages either way
+    static constexpr uint32_t kTmemCols = 2 * BN;          // two accumulators
+    static constexpr int kCols = BN / 2;                   // output columns per epilogue thread
+    static constexpr int kRedStride = BN + 4;  // row stride (floats) of the parked partial tile: 16-byte
+                                               // aligned rows, rows 4 banks apart (conflict-free v4)
+    static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
+    static_assert(BM * kRedStride * 4 <= kStages * kStageBytes, "partial tile must fit in the stages");
+};
 
 struct TcArgs {
     const float* sa;
@@ -70,28 +89,46 @@ __device__ __forceinline__ void flag_error(bool& failed, unsigned int code) {
 }
 
 template <bool kF32Out>
+__device__ __forceinline__ void store_one(void* out, int64_t idx, float v) {
+    if constexpr (kF32Out)
+        static_cast<float*>(out)[idx] = v;
+    else
+        static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+}
+
+// One CTA per SM. Ten warps share the SM's four register-file partitions
+// (three warps on two of them), which caps a thread at 168 registers.
+template <int BN, bool kF32Out>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                               const __grid_constant__ CUtensorMap tmap_b,
                                                               const TcArgs a) {
+    using C = TcCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
     uint8_t* const base_ptr = smem_raw + (base - ptx::smem_u32(smem_raw));
-    const uint32_t bar0 = base + kStages * kStageBytes;
-    const uint32_t full0 = bar0;                      // [kStages] TMA landed
-    const uint32_t empty0 = full0 + 8 * kStages;      // [kStages] MMAs done reading
-    const uint32_t tfull0 = empty0 + 8 * kStages;     // [2] accumulator ready
-    const uint32_t tempty0 = tfull0 + 16;             // [2] accumulator drained
+    const uint32_t bar0 = base + C::kStages * C::kStageBytes;
+    const uint32_t full0 = bar0;                       // [kStages] TMA landed
+    const uint32_t empty0 = full0 + 8 * C::kStages;    // [kStages] MMAs done reading
+    const uint32_t tfull0 = empty0 + 8 * C::kStages;   // [2] accumulator ready
+    const uint32_t tempty0 = tfull0 + 16;              // [2] accumulator drained
     const uint32_t tmem_slot = tempty0 + 16;
     volatile uint32_t* const tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM;
-    const int n0 = blockIdx.y * BN;
-    const int KB = a.KB;
+    const int mtiles = (a.M + BM - 1) / BM;
+    const int tiles = mtiles * ((a.N + BN - 1) / BN);
+    const int splits = gridDim.z;
+    const int split = blockIdx.z;  // == cluster rank when splits > 1 (cluster dims 1 x 1 x splits)
+    const int kb_begin = static_cast<int>(static_cast<int64_t>(split) * a.KB / splits);
+    const int kb_end = static_cast<int>(static_cast<int64_t>(split + 1) * a.KB / splits);
+    const int nk = kb_end - kb_begin;
+    // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ... (one when splitting K)
+    const int my_tiles = blockIdx.x < tiles ? (tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    const int total = my_tiles * nk;  // K groups this CTA streams
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(full0 + 8 * s, 1);
             ptx::mbar_init(empty0 + 8 * s, 1);
         }
@@ -102,13 +139,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
-        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_alloc(tmem_slot, C::kTmemCols);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
+
+    // epilogue geometry (warps 2..9)
+    const int qd = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int hf = (warp - 2) >> 2;           // column half
+    const int row = qd * 32 + lane;
+    float acc[C::kCols];
+    int m0 = (blockIdx.x % mtiles) * BM;   // tile of a split-K CTA (its only tile)
+    int n0 = (blockIdx.x / mtiles) * BN;
 
     if (warp == 0) {
         // ------------------------------------------------------- producer
@@ -118,20 +163,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             ptx::prefetch_tensormap(&tmap_b);
             const uint64_t policy = ptx::policy_evict_last();  // both operands are re-read by other tiles
             bool failed = false;
-            const int pre = KB < kStages ? KB : kStages;
+            // stage use i -> tile blockIdx.x + (i / nk) * gridDim.x, K group kb_begin + i % nk
+            auto tile_mn = [&](int i, int& m0_, int& n0_) {
+                const int tile = blockIdx.x + (i / nk) * gridDim.x;
+                m0_ = (tile % mtiles) * BM;
+                n0_ = (tile / mtiles) * BN;
+            };
+            const int pre = total < C::kStages ? total : C::kStages;
             for (int i = 0; i < pre; ++i) {  // weights: independent of the previous grid
-                ptx::mbar_arrive_expect_tx(full0 + 8 * i, kStageBytes);
-                ptx::tma_load_2d(base + i * kStageBytes + kABytes, &tmap_b, full0 + 8 * i, i * kGroup, n0, policy);
+                int m0_, n0_;
+                tile_mn(i, m0_, n0_);
+                ptx::mbar_arrive_expect_tx(full0 + 8 * i, C::kStageBytes);
+                ptx::tma_load_2d(base + i * C::kStageBytes + kABytes, &tmap_b, full0 + 8 * i,
+                                 (kb_begin + i % nk) * kGroup, n0_, policy);
             }
             ptx::griddep_wait();  // activations are the previous grid's output
-            for (int i = 0; i < pre; ++i)
-                ptx::tma_load_2d(base + i * kStageBytes, &tmap_a, full0 + 8 * i, i * kGroup, m0, policy);
-            for (int i = pre; i < KB; ++i) {
-                const int s = i % kStages;
-                if (!failed && !ptx::mbar_wait(empty0 + 8 * s, ((i / kStages) - 1) & 1)) flag_error(failed, 1u);
-                ptx::mbar_arrive_expect_tx(full0 + 8 * s, kStageBytes);
-                ptx::tma_load_2d(base + s * kStageBytes + kABytes, &tmap_b, full0 + 8 * s, i * kGroup, n0, policy);
-                ptx::tma_load_2d(base + s * kStageBytes, &tmap_a, full0 + 8 * s, i * kGroup, m0, policy);
+            for (int i = 0; i < pre; ++i) {
+                int m0_, n0_;
+                tile_mn(i, m0_, n0_);
+                ptx::tma_load_2d(base + i * C::kStageBytes, &tmap_a, full0 + 8 * i, (kb_begin + i % nk) * kGroup, m0_,
+                                 policy);
+            }
+            for (int i = pre; i < total; ++i) {
+                const int s = i % C::kStages;
+                int m0_, n0_;
+                tile_mn(i, m0_, n0_);
+                if (!failed && !ptx::mbar_wait(empty0 + 8 * s, ((i / C::kStages) - 1) & 1)) flag_error(failed, 1u);
+                ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
+                ptx::tma_load_2d(base + s * C::kStageBytes + kABytes, &tmap_b, full0 + 8 * s,
+                                 (kb_begin + i % nk) * kGroup, n0_, policy);
+                ptx::tma_load_2d(base + s * C::kStageBytes, &tmap_a, full0 + 8 * s, (kb_begin + i % nk) * kGroup, m0_,
+                                 policy);
             }
         }
     } else if (warp == 1) {
@@ -139,13 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_e4m3_f32(BM, BN);
             bool failed = false;
-            for (int i = 0; i < KB; ++i) {
-                const int s = i % kStages;
+            for (int i = 0; i < total; ++i) {
+                const int s = i % C::kStages;
                 const int b = i & 1;
-                if (!failed && !ptx::mbar_wait(full0 + 8 * s, (i / kStages) & 1)) flag_error(failed, 2u);
+                if (!failed && !ptx::mbar_wait(full0 + 8 * s, (i / C::kStages) & 1)) flag_error(failed, 2u);
                 if (i >= 2 && !failed && !ptx::mbar_wait(tempty0 + 8 * b, ((i >> 1) - 1) & 1)) flag_error(failed, 4u);
                 tc::fence_after_sync();
-                const uint32_t a_tile = base + s * kStageBytes;
+                const uint32_t a_tile = base + s * C::kStageBytes;
                 const uint32_t b_tile = a_tile + kABytes;
 #pragma unroll
                 for (int k = 0; k < kGroup / 32; ++k)
@@ -158,99 +220,224 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     } else {
         // ------------------------------------------------------- epilogue
         ptx::griddep_wait();  // scales come from the previous grid; it may still read `out`
-        const int qd = warp & 3;               // TMEM lane quadrant this warp may access
-        const int hf = (warp - 2) >> 2;        // column half: 0 for warps 2..5, 1 for warps 6..9
-        const int row = qd * 32 + lane;
-        const int m = m0 + row;
-        const int nb = n0 / kGroup + hf;
-        const bool row_ok = m < a.M && nb < a.NB;
-        const float* sa_row = a.sa + static_cast<int64_t>(row_ok ? m : 0) * KB;
-        const float* sw_row = a.sw + static_cast<int64_t>(row_ok ? nb : 0) * KB;
-        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + hf * 128;
-        float acc[128];
-#pragma unroll
-        for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + hf * C::kCols;
         bool failed = false;
-        for (int i = 0; i < KB; ++i) {
-            const int b = i & 1;
-            const float scale = row_ok ? __ldg(sa_row + i) * __ldg(sw_row + i) : 0.f;
-            if (!failed && !ptx::mbar_wait(tfull0 + 8 * b, (i >> 1) & 1)) flag_error(failed, 8u);
-            tc::fence_after_sync();
+        int i = 0;  // accumulator uses so far
+        for (int t = 0; t < my_tiles; ++t) {
+            const int tile = blockIdx.x + t * gridDim.x;
+            m0 = (tile % mtiles) * BM;
+            n0 = (tile / mtiles) * BN;
+            const int m = m0 + row;
+            const int nb = (n0 + hf * C::kCols) / kGroup;
+            const bool row_ok = m < a.M && nb < a.NB;
+            const float* sa_row = a.sa + static_cast<int64_t>(row_ok ? m : 0) * a.KB;
+            const float* sw_row = a.sw + static_cast<int64_t>(row_ok ? nb : 0) * a.KB;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tc::ld_32x32b_x32(t_row + b * BN + c * 32, r);
-                tc::wait_ld();
+            for (int j = 0; j < C::kCols; ++j) acc[j] = 0.f;
+            for (int k = 0; k < nk; ++k, ++i) {
+                const int b = i & 1;
+                const int kb = kb_begin + k;
+                const float scale = row_ok ? __ldg(sa_row + kb) * __ldg(sw_row + kb) : 0.f;
+                if (!failed && !ptx::mbar_wait(tfull0 + 8 * b, (i >> 1) & 1)) flag_error(failed, 8u);
+                tc::fence_after_sync();
+                if constexpr (C::kCols == 64) {
+                    // both 32-column halves in flight, one wait
+                    uint32_t r0[32], r1[32];
+                    tc::ld_32x32b_x32(t_row + b * BN, r0);
+                    tc::ld_32x32b_x32(t_row + b * BN + 32, r1);
+                    tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), scale, acc[c * 32 + j]);
-            }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(tempty0 + 8 * b);
-        }
-        // store this thread's 128-column row segment
-        if (m < a.M) {
-            const int nstart = n0 + hf * 128;
-            if constexpr (kF32Out) {
-                float* dst = static_cast<float*>(a.out) + static_cast<int64_t>(m) * a.N + nstart;
-                if ((a.N & 3) == 0 && nstart + 128 <= a.N) {
-#pragma unroll
-                    for (int j = 0; j < 128; j += 4)
-                        *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 128; ++j)
-                        if (nstart + j < a.N) dst[j] = acc[j];
-                }
-            } else {
-                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + static_cast<int64_t>(m) * a.N + nstart;
-                if ((a.N & 7) == 0 && nstart + 128 <= a.N) {
-#pragma unroll
-                    for (int j = 0; j < 128; j += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(acc[j], acc[j + 1]);
-                        v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-                        v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-                        v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-                        *reinterpret_cast<uint4*>(dst + j) = v;
+                    for (int j = 0; j < 32; ++j) {
+                        acc[j] = fmaf(__uint_as_float(r0[j]), scale, acc[j]);
+                        acc[32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[32 + j]);
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 128; ++j)
-                        if (nstart + j < a.N) dst[j] = __float2bfloat16_rn(acc[j]);
+                    for (int c = 0; c < C::kCols / 32; ++c) {
+                        uint32_t r[32];
+                        tc::ld_32x32b_x32(t_row + b * BN + c * 32, r);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), scale, acc[c * 32 + j]);
+                    }
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(tempty0 + 8 * b);
+            }
+            if (splits == 1 && m < a.M) {
+                // store this thread's row segment directly
+                const int nstart = n0 + hf * C::kCols;
+                if constexpr (kF32Out) {
+                    float* dst = static_cast<float*>(a.out) + static_cast<int64_t>(m) * a.N + nstart;
+                    if ((a.N & 3) == 0 && nstart + C::kCols <= a.N) {
+#pragma unroll
+                        for (int j = 0; j < C::kCols; j += 4)
+                            *reinterpret_cast<float4*>(dst + j) =
+                                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < C::kCols; ++j)
+                            if (nstart + j < a.N) dst[j] = acc[j];
+                    }
+                } else {
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + static_cast<int64_t>(m) * a.N + nstart;
+                    if ((a.N & 7) == 0 && nstart + C::kCols <= a.N) {
+#pragma unroll
+                        for (int j = 0; j < C::kCols; j += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(acc[j], acc[j + 1]);
+                            v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+                            v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+                            v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+                            *reinterpret_cast<uint4*>(dst + j) = v;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < C::kCols; ++j)
+                            if (nstart + j < a.N) dst[j] = __float2bfloat16_rn(acc[j]);
+                    }
                 }
             }
         }
+    }
+
+    if constexpr (BN == 128) {  // split K is only chosen with 128-wide tiles
+    if (splits > 1) {
+        // Park the partial tile in the idle stage memory (every MMA has
+        // completed and every TMA copy has landed: the epilogue saw the last
+        // accumulator), then reduce a slice of rows across the cluster.
+        float* red = reinterpret_cast<float*>(base_ptr);
+        if (warp >= 2) {
+#pragma unroll
+            for (int j = 0; j < C::kCols; j += 4)
+                *reinterpret_cast<float4*>(red + row * C::kRedStride + hf * C::kCols + j) =
+                    make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+        }
+        __syncwarp();  // barrier.cluster.*.aligned: the whole warp arrives together
+        ptx::cluster_sync();
+        if (warp >= 2) {
+            // 4 consecutive columns per element; every peer's load in flight before the sum
+            constexpr int kMaxSplits = 8;
+            const int r_begin = split * BM / splits;
+            const int r_end = (split + 1) * BM / splits;
+            const int tid = threadIdx.x - 64;
+            const int elems = (r_end - r_begin) * (BN / 4);
+            for (int e = tid; e < elems; e += kEpiWarps * 32) {
+                const int r = r_begin + e / (BN / 4);
+                const int col = 4 * (e % (BN / 4));
+                const uint32_t local = ptx::smem_u32(red + r * C::kRedStride + col);
+                float4 part[kMaxSplits];
+#pragma unroll
+                for (int c = 0; c < kMaxSplits; ++c)
+                    if (c < splits) part[c] = ptx::ld_shared_cluster_v4(ptx::mapa_shared(local, c));
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < kMaxSplits; ++c)
+                    if (c < splits) {
+                        v.x += part[c].x;
+                        v.y += part[c].y;
+                        v.z += part[c].z;
+                        v.w += part[c].w;
+                    }
+                const int m = m0 + r, n = n0 + col;
+                if (m < a.M) {
+                    const int64_t o = static_cast<int64_t>(m) * a.N + n;
+                    if (n + 3 < a.N && (a.N & 3) == 0) {
+                        if constexpr (kF32Out) {
+                            *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) = v;
+                        } else {
+                            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + o) =
+                                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+                        }
+                    } else {
+                        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (n + i < a.N) store_one<kF32Out>(a.out, o + i, vv[i]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        ptx::cluster_sync();  // no CTA leaves while its peers still read its shared memory
+    }
     }
 
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (warp == 1) tc::tmem_dealloc(tmem_base, kTmemCols);
+    if (warp == 1) tc::tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
-template <bool kF32Out>
-cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& args, cudaStream_t stream) {
-    auto kernel = gemm_tc_kernel<kF32Out>;
-    static std::atomic<uint64_t> configured{0};  // one bit per device
+template <int BN, bool kF32Out>
+cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& args, int num_sms,
+                         cudaStream_t stream) {
+    using C = TcCfg<BN>;
+    auto kernel = gemm_tc_kernel<BN, kF32Out>;
+    static std::atomic<uint64_t> configured{0};   // one bit per device
+    static std::atomic<int> max_clusters[64][9];  // per device and cluster size: 1 + clusters resident
     int dev = 0;
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
+    const int mt = (args.M + BM - 1) / BM;
+    const int nt = (args.N + BN - 1) / BN;
+    const int tiles = mt * nt;
+
+    // Split K over a cluster when the tiles leave SMs idle (128-wide tiles
+    // only): the largest S in 8..2 with at least 2 K groups per CTA, tiles * S
+    // CTAs within the SM count, and every cluster resident at once.
+    int splits = 1;
+    for (int s = 8; s >= 2 && BN == 128; --s) {
+        if (tiles * s > num_sms || args.KB < 2 * s) continue;
+        int cached = max_clusters[dev & 63][s].load(std::memory_order_relaxed);
+        if (cached == 0) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(1, 1, s);
+            q.blockDim = dim3(kThreads);
+            q.dynamicSmemBytes = C::kSmem;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = 1;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = s;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            cached = n + 1;
+            max_clusters[dev & 63][s].store(cached, std::memory_order_relaxed);
+        }
+        if (tiles <= cached - 1) {
+            splits = s;
+            break;
+        }
+    }
+
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((args.M + BM - 1) / BM, (args.N + BN - 1) / BN);
+    // split K: one CTA per (tile, split); otherwise persistent, one CTA per SM at most
+    cfg.gridDim = dim3(splits > 1 ? tiles : (tiles < num_sms ? tiles : num_sms), 1, splits);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = splits;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = splits > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, args);
 }
 
@@ -270,7 +457,7 @@ unsigned int read_and_clear_tc_error() {
 }
 
 cudaError_t launch_gemm_tc(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N, int K,
-                           void* out, bool out_f32, cudaStream_t stream) {
+                           void* out, bool out_f32, int num_sms, cudaStream_t stream) {
     TcArgs a;
     a.sa = sa;
     a.sw = sw;
@@ -280,13 +467,23 @@ cudaError_t launch_gemm_tc(const uint8_t* q, const float* sa, const uint8_t* w, 
     a.K = K;
     a.KB = K / kGroup;
     a.NB = (N + kGroup - 1) / kGroup;
+    // 256-wide weight tiles when the grid is large (prefill: fewer operand
+    // re-reads per FLOP); 128-wide ones otherwise (twice the tiles to spread
+    // a batched-decode weight stream over the SMs).
+    const int mt = (M + BM - 1) / BM;
+    const bool wide = static_cast<int64_t>(mt) * ((N + 255) / 256) >= 2 * num_sms;
+    const int bn = wide ? 256 : 128;
     CUtensorMap ta, tb;
     if (!encode_tmap_2d_u8(&ta, q, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K),
                            kGroup, BM, true) ||
         !encode_tmap_2d_u8(&tb, w, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K),
-                           kGroup, BN, true))
+                           kGroup, bn, true))
         return cudaErrorInvalidValue;
-    return out_f32 ? launch_typed<true>(ta, tb, a, stream) : launch_typed<false>(ta, tb, a, stream);
+    if (wide)
+        return out_f32 ? launch_typed<256, true>(ta, tb, a, num_sms, stream)
+                       : launch_typed<256, false>(ta, tb, a, num_sms, stream);
+    return out_f32 ? launch_typed<128, true>(ta, tb, a, num_sms, stream)
+                   : launch_typed<128, false>(ta, tb, a, num_sms, stream);
 }
 
 }  // namespace fp8act

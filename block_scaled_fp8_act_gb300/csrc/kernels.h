@@ -25,10 +25,11 @@ cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const u
                                       int N, int K, void* out, bool out_f32, int num_sms, int unroll,
                                       cudaStream_t stream);
 
-// Tensor-memory (tcgen05) GEMM: 128 x 256 output tiles, TMA-fed 4-stage
-// ring, per-K-group promotion of the fp32 block scales in the epilogue.
+// Tensor-memory (tcgen05) GEMM: 128 x 256 (prefill) or 128 x 128 output
+// tiles, TMA-fed ring, per-K-group promotion of the fp32 block scales in the
+// epilogue, split K over a thread-block cluster when the tiles are too few.
 cudaError_t launch_gemm_tc(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N, int K,
-                           void* out, bool out_f32, cudaStream_t stream);
+                           void* out, bool out_f32, int num_sms, cudaStream_t stream);
 
 // Device-side error word of the tcgen05 kernel (non-zero after a bounded
 // wait gave up); reading it synchronises with the device and clears it.
