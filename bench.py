@@ -346,7 +346,7 @@ def sweep(weights, device, stream, peaks) -> dict:
     """us/call of the block GEMM per shape at every workload M (outside the timed step)."""
     res = {}
     hbm = peaks["hbm_gbs"]
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    fp8_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
     for M in (1, 2, 3, 4, 5, 6, 7, 8, 64, 102, 4096):
         wl = Workload(M, weights, device)
         ts = gemm_kernel_times(wl, stream, launches=30 if M <= 102 else 3, reps=3)
@@ -466,8 +466,11 @@ def main() -> None:
     traffic = recorded_traffic(kernel, f"{args.workload}_m{M}_mean_of_5")
     if bound == "tensor":
         achieved = sum(gemm_flops) / sum(gemm_ts) / 1e12
-        peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
-        peak_kind = (f"{peaks_kind} bf16 dense (cuBLAS, burst) x {FP8_OVER_BF16:g}, the nominal FP8/bf16 ratio")
+        # a millisecond-long GEMM inside a long step runs under the power cap:
+        # the sustained bf16 rate (seconds-long cuBLAS loop) is its reference
+        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * FP8_OVER_BF16
+        peak_kind = (f"{peaks_kind} bf16 dense (cuBLAS, sustained under the power cap) x {FP8_OVER_BF16:g}, "
+                     "the nominal FP8/bf16 ratio")
         roof_unit, per_launch = "TFLOP/s", {"flops_per_launch": sum(gemm_flops) / len(gemm_flops)}
         per_shape = [{"N": N, "K": K, "us_per_call": round(t * 1e6, 3), "tflops": round(f / t / 1e12, 1),
                       "frac": round(f / t / 1e12 / peak, 4)}

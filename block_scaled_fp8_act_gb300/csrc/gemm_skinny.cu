@@ -164,31 +164,49 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
     }
 }
 
-// Warps per CTA: the largest divisor of K/128 (<= kMaxWarps) for which the
-// whole grid is resident at once (one wave: every warp has the same number of
-// K blocks, so all of them finish together), else the smallest grid-friendly
-// choice of 4 warps. Occupancy answers are cached per (device, warps).
+// CTAs per SM for a (load depth, token groups, warps) configuration, from the
+// occupancy API, cached per device.
 template <bool kF32Out, int kUnroll, int kTG>
-int pick_warps(int64_t ctas, int KB, int num_sms) {
-    static std::atomic<int> per_sm_cache[64][kMaxWarps + 1];  // 0 = unknown, else 1 + CTAs per SM
+int ctas_per_sm(int wv) {
+    static std::atomic<int> cache[64][kMaxWarps + 1];  // 0 = unknown, else 1 + CTAs per SM
     int dev = 0;
     cudaGetDevice(&dev);
-    for (int wv = kMaxWarps; wv >= 1; --wv) {
-        if (wv > KB || KB % wv) continue;
-        int cached = per_sm_cache[dev & 63][wv].load(std::memory_order_relaxed);
-        if (cached == 0) {
-            int per_sm = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out, kUnroll, kTG>, 32 * wv,
-                                                              0) != cudaSuccess) {
-                cudaGetLastError();
-                break;
-            }
-            cached = per_sm + 1;
-            per_sm_cache[dev & 63][wv].store(cached, std::memory_order_relaxed);
+    int cached = cache[dev & 63][wv].load(std::memory_order_relaxed);
+    if (cached == 0) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out, kUnroll, kTG>, 32 * wv,
+                                                          0) != cudaSuccess) {
+            cudaGetLastError();
+            per_sm = 0;
         }
-        if (ctas <= static_cast<int64_t>(cached - 1) * num_sms) return wv;
+        cached = per_sm + 1;
+        cache[dev & 63][wv].store(cached, std::memory_order_relaxed);
     }
-    return KB < 4 ? KB : 4;
+    return cached - 1;
+}
+
+// Warps per CTA for a load depth: among the warp counts whose K groups split
+// evenly to within 10% (every warp finishes at about the same time) and for
+// which the whole grid is resident in one wave, the one with the most weight
+// bytes in flight (capped where HBM saturates, ~20 MB on GB300); 0 if none.
+template <bool kF32Out, int kUnroll, int kTG>
+int pick_warps(int64_t ctas, int KB, int num_sms, int64_t* inflight_out) {
+    constexpr int64_t kSaturate = int64_t(20) << 20;
+    int best = 0;
+    int64_t best_inflight = -1;
+    for (int wv = 1; wv <= kMaxWarps && wv <= KB; ++wv) {
+        const int per_warp = (KB + wv - 1) / wv;
+        if (10 * KB < 9 * wv * per_warp) continue;  // warps would finish more than 10% apart
+        if (ctas > static_cast<int64_t>(ctas_per_sm<kF32Out, kUnroll, kTG>(wv)) * num_sms) continue;
+        int64_t inflight = ctas * wv * (per_warp < kUnroll ? per_warp : kUnroll) * (16 * kGroup);
+        if (inflight > kSaturate) inflight = kSaturate;
+        if (inflight > best_inflight || (inflight == best_inflight && wv < best)) {
+            best = wv;
+            best_inflight = inflight;
+        }
+    }
+    if (inflight_out) *inflight_out = best_inflight;
+    return best;
 }
 
 template <bool kF32Out, int kUnroll, int kTG>
@@ -199,7 +217,9 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
     const int64_t ctas = static_cast<int64_t>(grid.x) * grid.y;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(32 * pick_warps<kF32Out, kUnroll, kTG>(ctas, KB, num_sms));
+    int wv = pick_warps<kF32Out, kUnroll, kTG>(ctas, KB, num_sms, nullptr);
+    if (wv == 0) wv = KB < 4 ? KB : 4;  // grid larger than one wave: plain 4-warp CTAs
+    cfg.blockDim = dim3(32 * wv);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -226,16 +246,22 @@ cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const u
 
 cudaError_t launch_gemm_skinny(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
                                int N, int K, void* out, bool out_f32, int num_sms, cudaStream_t stream) {
-    // Load depth: a warp that streams >= 8 K blocks keeps 4 of them in flight
-    // (fewer warps fit, but each covers more of the latency); shorter K
-    // ranges keep 2 and more warps. The warp count comes from the depth-2
-    // configuration's single-wave rule.
+    // Load depth: 4 K groups in flight per warp (128 registers, fewer warps)
+    // when that puts more bytes in flight than depth 2; short K (< 32 groups)
+    // keeps depth 2, which measured faster there (more, shorter warps).
     int unroll = 2;
     if (M <= 8) {
         const int KB = K / kGroup;
         const int64_t ctas = (N + 15) / 16;
-        const int wv = out_f32 ? pick_warps<true, 2, 1>(ctas, KB, num_sms) : pick_warps<false, 2, 1>(ctas, KB, num_sms);
-        if (KB / wv >= 8) unroll = 4;
+        int64_t in2 = 0, in4 = 0;
+        if (out_f32) {
+            pick_warps<true, 2, 1>(ctas, KB, num_sms, &in2);
+            pick_warps<true, 4, 1>(ctas, KB, num_sms, &in4);
+        } else {
+            pick_warps<false, 2, 1>(ctas, KB, num_sms, &in2);
+            pick_warps<false, 4, 1>(ctas, KB, num_sms, &in4);
+        }
+        if (KB >= 32 && in4 > in2) unroll = 4;
     }
     return launch_gemm_skinny_unroll(q, sa, w, sw, M, N, K, out, out_f32, num_sms, unroll, stream);
 }

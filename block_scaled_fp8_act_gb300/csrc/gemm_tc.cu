@@ -59,10 +59,21 @@ namespace {
 constexpr int BM = 128;  // tokens per tile (TMEM lanes)
 constexpr int kABytes = BM * kGroup;  // 16 KB
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps) * 32;
 
 template <int BN>
 struct TcCfg {
+    // Warp roles: warp 0 TMA producer, warp 1 MMA issuer, then the eight
+    // epilogue warps. The 256-wide tile runs 12 warps (three warpgroups) so
+    // that warpgroup 0 (producer, MMA, two idle warps) can hand registers to
+    // the two epilogue warpgroups with setmaxnreg: 128 x 56 + 256 x 224 =
+    // 64512 = 384 x 168, exactly the launch's registers.
+    static constexpr int kCtrlWarps = BN == 256 ? 4 : 2;
+    static constexpr int kThreads = (kCtrlWarps + kEpiWarps) * 32;
+    static constexpr int kRegsLaunch = 168;  // per thread at launch (ptxas, __launch_bounds__)
+    static constexpr int kRegsCtrl = 56;
+    static constexpr int kRegsEpi = 224;
+    static_assert(BN != 256 || 128 * kRegsCtrl + 256 * kRegsEpi <= kThreads * kRegsLaunch,
+                  "register split exceeds the launch's registers");
     static constexpr int kBBytes = BN * kGroup;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kStages = BN == 256 ? 4 : 6;    // ~192 KB of stages either way
@@ -99,7 +110,7 @@ __device__ __forceinline__ void store_one(void* out, int64_t idx, float v) {
 // One CTA per SM. Ten warps share the SM's four register-file partitions
 // (three warps on two of them), which caps a thread at 168 registers.
 template <int BN, bool kF32Out>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
+__global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                               const __grid_constant__ CUtensorMap tmap_b,
                                                               const TcArgs a) {
     using C = TcCfg<BN>;
@@ -147,14 +158,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
 
-    // epilogue geometry (warps 2..9)
-    const int qd = warp & 3;                  // TMEM lane quadrant this warp may access
-    const int hf = (warp - 2) >> 2;           // column half
+    // epilogue geometry (warps kCtrlWarps .. kCtrlWarps + 7)
+    const bool epi = warp >= C::kCtrlWarps;
+    const int qd = warp & 3;                          // TMEM lane quadrant this warp may access
+    const int hf = (warp - C::kCtrlWarps) >> 2;       // column half
     const int row = qd * 32 + lane;
     float acc[C::kCols];
     int m0 = (blockIdx.x % mtiles) * BM;   // tile of a split-K CTA (its only tile)
     int n0 = (blockIdx.x / mtiles) * BN;
 
+    if (!epi) {
+    if constexpr (BN == 256) tc::regs_decrease<C::kRegsCtrl>();
     if (warp == 0) {
         // ------------------------------------------------------- producer
         if (lane == 0) {
@@ -217,8 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 tc::commit(tfull0 + 8 * b);   // the accumulator holds this K group's product
             }
         }
+    }
     } else {
         // ------------------------------------------------------- epilogue
+        if constexpr (BN == 256) tc::regs_increase<C::kRegsEpi>();
         ptx::griddep_wait();  // scales come from the previous grid; it may still read `out`
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + hf * C::kCols;
         bool failed = false;
@@ -247,19 +263,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     tc::ld_32x32b_x32(t_row + b * BN + 32, r1);
                     tc::wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        acc[j] = fmaf(__uint_as_float(r0[j]), scale, acc[j]);
-                        acc[32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[32 + j]);
+                    for (int j = 0; j < 32; j += 2) {
+                        tc::ffma2(acc[j], acc[j + 1], r0[j], r0[j + 1], scale);
+                        tc::ffma2(acc[32 + j], acc[33 + j], r1[j], r1[j + 1], scale);
                     }
                 } else {
+                    // two rounds of 64 columns, both 32-column loads of a round in flight
 #pragma unroll
-                    for (int c = 0; c < C::kCols / 32; ++c) {
-                        uint32_t r[32];
-                        tc::ld_32x32b_x32(t_row + b * BN + c * 32, r);
+                    for (int c = 0; c < C::kCols / 64; ++c) {
+                        uint32_t r0[32], r1[32];
+                        tc::ld_32x32b_x32(t_row + b * BN + c * 64, r0);
+                        tc::ld_32x32b_x32(t_row + b * BN + c * 64 + 32, r1);
                         tc::wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), scale, acc[c * 32 + j]);
+                        for (int j = 0; j < 32; j += 2) {
+                            tc::ffma2(acc[c * 64 + j], acc[c * 64 + j + 1], r0[j], r0[j + 1], scale);
+                            tc::ffma2(acc[c * 64 + 32 + j], acc[c * 64 + 33 + j], r1[j], r1[j + 1], scale);
+                        }
                     }
                 }
                 tc::fence_before_sync();
@@ -309,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         // completed and every TMA copy has landed: the epilogue saw the last
         // accumulator), then reduce a slice of rows across the cluster.
         float* red = reinterpret_cast<float*>(base_ptr);
-        if (warp >= 2) {
+        if (epi) {
 #pragma unroll
             for (int j = 0; j < C::kCols; j += 4)
                 *reinterpret_cast<float4*>(red + row * C::kRedStride + hf * C::kCols + j) =
@@ -317,12 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         __syncwarp();  // barrier.cluster.*.aligned: the whole warp arrives together
         ptx::cluster_sync();
-        if (warp >= 2) {
+        if (epi) {
             // 4 consecutive columns per element; every peer's load in flight before the sum
             constexpr int kMaxSplits = 8;
             const int r_begin = split * BM / splits;
             const int r_end = (split + 1) * BM / splits;
-            const int tid = threadIdx.x - 64;
+            const int tid = threadIdx.x - 32 * C::kCtrlWarps;
             const int elems = (r_end - r_begin) * (BN / 4);
             for (int e = tid; e < elems; e += kEpiWarps * 32) {
                 const int r = r_begin + e / (BN / 4);
@@ -384,6 +404,14 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const TcA
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
+        if constexpr (BN == 256) {
+            // setmaxnreg.inc waits for registers the block does not have if the
+            // compiler allocated fewer than the split assumes: refuse to launch.
+            cudaFuncAttributes fa{};
+            e = cudaFuncGetAttributes(&fa, kernel);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
+        }
         configured.fetch_or(bit, std::memory_order_release);
     }
     const int mt = (args.M + BM - 1) / BM;
@@ -400,7 +428,7 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const TcA
         if (cached == 0) {
             cudaLaunchConfig_t q = {};
             q.gridDim = dim3(1, 1, s);
-            q.blockDim = dim3(kThreads);
+            q.blockDim = dim3(C::kThreads);
             q.dynamicSmemBytes = C::kSmem;
             cudaLaunchAttribute qa[1];
             qa[0].id = cudaLaunchAttributeClusterDimension;
@@ -426,7 +454,7 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const TcA
     cudaLaunchConfig_t cfg = {};
     // split K: one CTA per (tile, split); otherwise persistent, one CTA per SM at most
     cfg.gridDim = dim3(splits > 1 ? tiles : (tiles < num_sms ? tiles : num_sms), 1, splits);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
