@@ -263,9 +263,9 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                     tc::ld_32x32b_x32(t_row + b * BN + 32, r1);
                     tc::wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        tc::ffma2(acc[j], acc[j + 1], r0[j], r0[j + 1], scale);
-                        tc::ffma2(acc[32 + j], acc[33 + j], r1[j], r1[j + 1], scale);
+                    for (int j = 0; j < 32; ++j) {
+                        acc[j] = fmaf(__uint_as_float(r0[j]), scale, acc[j]);
+                        acc[32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[32 + j]);
                     }
                 } else {
                     // two rounds of 64 columns, both 32-column loads of a round in flight
@@ -276,9 +276,9 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                         tc::ld_32x32b_x32(t_row + b * BN + c * 64 + 32, r1);
                         tc::wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            tc::ffma2(acc[c * 64 + j], acc[c * 64 + j + 1], r0[j], r0[j + 1], scale);
-                            tc::ffma2(acc[c * 64 + 32 + j], acc[c * 64 + 33 + j], r1[j], r1[j + 1], scale);
+                        for (int j = 0; j < 32; ++j) {
+                            acc[c * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[c * 64 + j]);
+                            acc[c * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[c * 64 + 32 + j]);
                         }
                     }
                 }

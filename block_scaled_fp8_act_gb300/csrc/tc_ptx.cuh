@@ -86,21 +86,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// Two fp32 FMAs in one instruction (a0, a1) += (x0, x1) * s, each rounded to
-// nearest exactly like fmaf.
-__device__ __forceinline__ void ffma2(float& a0, float& a1, uint32_t x0, uint32_t x1, float s) {
-    asm("{\n"
-        ".reg .b64 acc, xv, sv;\n"
-        "mov.b64 acc, {%0, %1};\n"
-        "mov.b64 xv, {%2, %3};\n"
-        "mov.b64 sv, {%4, %4};\n"
-        "fma.rn.f32x2 acc, xv, sv, acc;\n"
-        "mov.b64 {%0, %1}, acc;\n"
-        "}\n"
-        : "+f"(a0), "+f"(a1)
-        : "r"(x0), "r"(x1), "f"(s));
-}
-
 // Warpgroup register reallocation: every warp of the warpgroup executes it.
 // Decrease gives registers back to the CTA's pool; increase waits until the
 // pool can cover the new per-thread count.
