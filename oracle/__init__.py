@@ -59,6 +59,7 @@ def _load():
             lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
             lib.oracle_bf16_from_double.restype = ctypes.c_uint16
             lib.oracle_block_gemm_rows.argtypes = [p, p, p, p, i64, i64, i64, p, i64, p, p, p]
+            lib.oracle_block_gemm_w8a16_rows.argtypes = [p, p, p, i64, i64, i64, p, i64, p, p, p]
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -153,4 +154,31 @@ def block_gemm(q, sa, w, sw, rows=None):
     _check(_load().oracle_block_gemm_rows(_ptr(q), _ptr(sa), _ptr(w), _ptr(sw), M, N, K,
                                           rows_p, R if rows is not None else 0,
                                           _ptr(y), _ptr(aabs), _ptr(out)), "block_gemm")
+    return y, aabs, out
+
+
+def block_gemm_w8a16(x_bits, w, sw, rows=None):
+    """Weight-only block-FP8 GEMM: bf16 activations (raw uint16 bits [M, K])
+    times E4M3 weights with 128x128 fp32 block scales, no activation quant.
+
+    Returns (y float64 [R, N], aabs float64 [R, N], out bf16 bits uint16 [R, N]).
+    """
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint8)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or sw.shape != ((N + G - 1) // G, K // G):
+        raise OracleError("block_gemm_w8a16: inconsistent shapes")
+    if rows is None:
+        R, rows_p = M, None
+    else:
+        keep = np.ascontiguousarray(rows, dtype=np.int64)
+        R, rows_p = keep.size, _ptr(keep)
+    y = np.empty((R, N), np.float64)
+    aabs = np.empty((R, N), np.float64)
+    out = np.empty((R, N), np.uint16)
+    _check(_load().oracle_block_gemm_w8a16_rows(_ptr(x), _ptr(w), _ptr(sw), M, N, K, rows_p,
+                                                R if rows is not None else 0, _ptr(y), _ptr(aabs), _ptr(out)),
+           "block_gemm_w8a16")
     return y, aabs, out

@@ -31,7 +31,10 @@
  * and the format's closed-form landmarks, the encoder against torch's
  * converter and hand-derived ties, the quantisers against exact rational
  * checks, and the GEMM against exact Fraction brute force, one-hot inputs,
- * scale linearity and K permutation.
+ * scale linearity and K permutation. The weight-only GEMM is pinned by
+ * Fraction brute force, by its exact reduction to the W8A8 GEMM when the
+ * activations are quantised values times powers of two, and by an fp64
+ * dequantise-then-matmul.
  *
  * Built with gcc -O2 -fopenmp (no fast-math: IEEE fp32 division and no
  * flush-to-zero are part of the definition).
@@ -266,6 +269,60 @@ int oracle_block_gemm_rows(const uint8_t* q, const float* sa, const uint8_t* w, 
 int oracle_block_gemm(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw,
                       int64_t M, int64_t N, int64_t K, double* y, double* aabs, uint16_t* out) {
     return oracle_block_gemm_rows(q, sa, w, sw, M, N, K, NULL, 0, y, aabs, out);
+}
+
+/*
+ * Weight-only block-FP8 GEMM (W8A16) for the listed output rows: the same
+ * E4M3 weights and 128x128 block scales, multiplied by the bf16 activations
+ * themselves, with no activation quantisation. This is the job of the
+ * weight-only FP8 back-end (Marlin) that the single-RTX-PRO-6000
+ * Qwen3.8-27B optimisation post chooses at one request, section "单并发优化",
+ * because it skips the activation quantisation. The pages give no formula;
+ * the plain reading is the dequantised product:
+ *   y[m][n] = sum_kb sw[n/G][kb] * sum_{k in kb} x[m][k] * dq(w[n][k]).
+ * x is bf16 bits [M, K]; w, sw, rows, y, aabs, out as in
+ * oracle_block_gemm_rows (aabs = sum_kb |sw * block dot|). Each product
+ * bf16 * E4M3 has at most 12 significant bits, so the fp64 block dot is
+ * exact while one block's products span less than 2^41 in magnitude (true
+ * of every test input); the block scales and the sum over blocks are fp64.
+ */
+int oracle_block_gemm_w8a16_rows(const uint16_t* x, const uint8_t* w, const float* sw, int64_t M, int64_t N,
+                                 int64_t K, const int64_t* rows, int64_t nrows, double* y, double* aabs,
+                                 uint16_t* out) {
+    if (M < 0 || N < 0 || K < 0 || K % G || nrows < 0) return ORACLE_ERR_SHAPE;
+    build_table();
+    int64_t KB = K / G;
+    if (rows == NULL) nrows = M;
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        if (m < 0 || m >= M) return ORACLE_ERR_SHAPE;
+        for (int64_t k = 0; k < K; ++k)
+            if (!isfinite(bf16_to_float(x[m * K + k]))) return ORACLE_ERR_NONFINITE;
+    }
+    for (int64_t i = 0; i < N * K; ++i)
+        if ((w[i] & 0x7F) == 0x7F) return ORACLE_ERR_NAN_CODE;
+
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t i = 0; i < nrows; ++i)
+        for (int64_t n = 0; n < N; ++n) {
+            int64_t m = rows ? rows[i] : i;
+            const uint16_t* xr = x + m * K;
+            const uint8_t* wr = w + n * K;
+            const float* sw_row = sw + (n / G) * KB; /* scales of this row's 128-row weight block */
+            double sum = 0.0, sum_abs = 0.0;
+            for (int64_t kb = 0; kb < KB; ++kb) {
+                double dot = 0.0;
+                for (int64_t k = kb * G; k < (kb + 1) * G; ++k)
+                    dot += (double)bf16_to_float(xr[k]) * (double)e4m3_value[wr[k]];
+                double t = (double)sw_row[kb] * dot;
+                sum += t;
+                sum_abs += fabs(t);
+            }
+            if (y) y[i * N + n] = sum;
+            if (aabs) aabs[i * N + n] = sum_abs;
+            if (out) out[i * N + n] = oracle_bf16_from_double(sum);
+        }
+    return ORACLE_OK;
 }
 
 /* Threads the OpenMP loops use (1 when built without OpenMP). */

@@ -36,6 +36,10 @@ MUTANTS = {
     "gemm_abs_sign": ("acc += term;", "acc += fabs(term);"),
     "bf16_double_rounding": ("frexp(y, &e);", "y = (double)(float)y; frexp(y, &e);"),
     "bf16_truncates": ("nearbyint(ldexp(y, -qe))", "trunc(ldexp(y, -qe))"),
+    "w8a16_sw_ignores_row_block": ("sw_row = sw + (n / G) * KB;", "sw_row = sw;"),
+    "w8a16_drops_activation_sign": ("dot += (double)bf16_to_float(xr[k])", "dot += fabs((double)bf16_to_float(xr[k]))"),
+    "w8a16_drops_last_block_element": ("for (int64_t k = kb * G; k < (kb + 1) * G; ++k)\n                    dot",
+                                       "for (int64_t k = kb * G; k < (kb + 1) * G - 1; ++k)\n                    dot"),
 }
 
 

@@ -375,3 +375,67 @@ def test_projection_shapes_fixture():
             if line.strip() and not line.startswith("#")]
     assert tuple(rows) == inputs.SHAPES
     assert all(K % G == 0 and N % G == 0 for N, K in rows)
+
+
+# ------------------------------------------------- weight-only GEMM (W8A16)
+def _w8a16_problem(M, N, K, seed):
+    x = inputs.activations_bf16(M, K, seed=seed)
+    W = inputs.weights_bf16(N, K, seed=seed + 1)
+    w, sw = oracle.weight_quant(inputs.bf16_bits(W))
+    return x, w, sw
+
+
+def test_w8a16_brute_force_fractions():
+    """Exact rational y (bf16 x times torch-decoded weights) on a tiny problem
+    with two scale blocks along N and K."""
+    M, N, K = 2, 200, 256
+    x, w, sw = _w8a16_problem(M, N, K, seed=141)
+    y, aabs, out = oracle.block_gemm_w8a16(inputs.bf16_bits(x), w, sw)
+    xf = x.float().numpy()          # bf16 -> fp32 is exact
+    dq_w = torch_e4m3_decode(w)
+    for m in range(M):
+        for n in range(N):
+            exact = Fraction(0)
+            for kb in range(K // G):
+                dot = sum(Fraction(float(xf[m, k])) * Fraction(float(dq_w[n, k])) for k in range(kb * G, (kb + 1) * G))
+                exact += Fraction(float(sw[n // G, kb])) * dot
+            assert abs(Fraction(float(y[m, n])) - exact) <= Fraction(2.0 ** -50) * Fraction(float(aabs[m, n]))
+            assert out[m, n] == bf16_rne_fraction(exact)
+
+
+def test_w8a16_reduces_to_w8a8_on_quantised_activations():
+    """When x is itself dq(q) * sa with power-of-two sa (exact in bf16), the
+    weight-only product equals the W8A8 block GEMM of (q, sa) exactly."""
+    M, N, K = 3, 256, 384
+    rng = np.random.default_rng(7)
+    q = rng.integers(0, 256, size=(M, K), dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x3C                      # no NaN codes
+    sa = (2.0 ** rng.integers(-6, 4, size=(M, K // G))).astype(np.float32)
+    xf = torch_e4m3_decode(q).astype(np.float64) * np.repeat(sa.astype(np.float64), G, axis=1)
+    x = torch.from_numpy(xf).to(torch.bfloat16)
+    assert np.array_equal(x.double().numpy(), xf)     # the bf16 activations are exact
+    W = inputs.weights_bf16(N, K, seed=143)
+    w, sw = oracle.weight_quant(inputs.bf16_bits(W))
+    y16, a16, o16 = oracle.block_gemm_w8a16(inputs.bf16_bits(x), w, sw)
+    y8, a8, o8 = oracle.block_gemm(q, sa, w, sw)
+    assert np.array_equal(y16, y8) and np.array_equal(a16, a8) and np.array_equal(o16, o8)
+
+
+def test_w8a16_matches_float64_dequant_matmul_and_rows():
+    M, N, K = 6, 300, 512
+    x, w, sw = _w8a16_problem(M, N, K, seed=151)
+    y, _, o = oracle.block_gemm_w8a16(inputs.bf16_bits(x), w, sw)
+    X = x.double()
+    Wd = torch.from_numpy(torch_e4m3_decode(w)).double()
+    ref = torch.zeros(M, N, dtype=torch.float64)
+    for kb in range(K // G):
+        part = X[:, kb * G:(kb + 1) * G] @ Wd[:, kb * G:(kb + 1) * G].T
+        ref += part * torch.from_numpy(sw[:, kb].astype(np.float64)).repeat_interleave(G)[:N][None, :]
+    assert torch.allclose(torch.from_numpy(y), ref, rtol=1e-12, atol=1e-12)
+    rows = np.array([4, 1])
+    ys, _, os_ = oracle.block_gemm_w8a16(inputs.bf16_bits(x), w, sw, rows=rows)
+    assert np.array_equal(ys, y[rows]) and np.array_equal(os_, o[rows])
+    xb = inputs.bf16_bits(x).copy()
+    xb[0, 3] = 0x7FC0                                  # a bf16 NaN
+    with pytest.raises(oracle.OracleError):
+        oracle.block_gemm_w8a16(xb, w, sw)
