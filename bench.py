@@ -19,6 +19,9 @@ Printed JSON line (rank 0):
   sweep      us/call per shape at M = 1..8 (the no-cliff check), 64, 102
              and 4096 (the last as TFLOP/s of FP8 tensor peak)
 
+`--workload verify|batched|prefill` times the same step at M = 8, 102 or
+4096; `--workload decode-w8a16` times the weight-only variant at M = 1 (bf16
+activations straight into the GEMM, no quantisation launch).
 `--impl reference` times the CPU oracle instead (the reference arm).
 """
 from __future__ import annotations
@@ -54,7 +57,10 @@ WORKLOADS = {
                      "(act quant + block-FP8 GEMM per shape)", "hbm"),
     "prefill": (4096, "prefill chunk M={M} over the five dense-27B projection shapes "
                       "(act quant + block-FP8 GEMM per shape)", "tensor"),
+    "decode-w8a16": (1, "weight-only decode M={M} over the five dense-27B projection shapes "
+                        "(bf16 activations x block-FP8 weights, one GEMM per shape, no act quant)", "hbm"),
 }
+WEIGHT_ONLY = {"decode-w8a16"}
 
 
 def gemm_kernel_name(M: int) -> str:
@@ -70,6 +76,12 @@ def algorithmic_gemm_bytes(M: int, N: int, K: int) -> int:
     scales of the activations, and the bf16 output."""
     KB, NB = K // G, (N + G - 1) // G
     return N * K + 4 * NB * KB + M * K + 4 * M * KB + 2 * M * N
+
+
+def algorithmic_w8a16_bytes(M: int, N: int, K: int) -> int:
+    """Weight-only GEMM: weights + scales, bf16 activations, bf16 output."""
+    KB, NB = K // G, (N + G - 1) // G
+    return N * K + 4 * NB * KB + 2 * M * K + 2 * M * N
 
 
 def algorithmic_quant_bytes(M: int, K: int) -> int:
@@ -193,8 +205,9 @@ class Workload:
     """Device-resident activations of one M over the five shapes (plus pinned
     host copies for the end-to-end leg), sharing one Weights set."""
 
-    def __init__(self, M: int, weights: Weights, device: torch.device):
+    def __init__(self, M: int, weights: Weights, device: torch.device, weight_only: bool = False):
         self.M = M
+        self.weight_only = weight_only
         self.shapes = weights.shapes
         self.copies = weights.copies
         self.w, self.sw = weights.w, weights.sw
@@ -210,19 +223,31 @@ class Workload:
             self.out_host.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
         torch.cuda.synchronize()
 
+    def gemm_bytes_of(self, N: int, K: int) -> int:
+        return (algorithmic_w8a16_bytes if self.weight_only else algorithmic_gemm_bytes)(self.M, N, K)
+
     def step_bytes(self) -> int:
-        return sum(algorithmic_gemm_bytes(self.M, N, K) + algorithmic_quant_bytes(self.M, K)
+        return sum(self.gemm_bytes_of(N, K) + (0 if self.weight_only else algorithmic_quant_bytes(self.M, K))
                    for N, K in self.shapes)
 
-    def gemm_bytes(self) -> int:
-        return sum(algorithmic_gemm_bytes(self.M, N, K) for N, K in self.shapes)
+    def launches_per_step(self) -> int:
+        return (1 if self.weight_only else 2) * len(self.shapes)
+
+    def gemm(self, si: int, copy: int, stream) -> None:
+        from block_scaled_fp8_act_gb300 import fp8act
+        if self.weight_only:
+            fp8act.fp8_block_gemm_w8a16(self.x[si], self.w[si][copy], self.sw[si][copy], self.out[si],
+                                        stream=stream)
+        else:
+            fp8act.fp8_block_gemm(self.q[si], self.sa[si], self.w[si][copy], self.sw[si][copy],
+                                  self.out[si], stream=stream)
 
     def enqueue_step(self, copy: int, stream) -> None:
         from block_scaled_fp8_act_gb300 import fp8act
         for si in range(len(self.shapes)):
-            fp8act.fp8_act_quant(self.x[si], self.q[si], self.sa[si], stream=stream)
-            fp8act.fp8_block_gemm(self.q[si], self.sa[si], self.w[si][copy], self.sw[si][copy],
-                                  self.out[si], stream=stream)
+            if not self.weight_only:
+                fp8act.fp8_act_quant(self.x[si], self.q[si], self.sa[si], stream=stream)
+            self.gemm(si, copy, stream)
 
 
 def capture(fn, stream) -> torch.cuda.CUDAGraph:
@@ -251,16 +276,14 @@ def time_graphs(graphs, steps: int, warmup: int, stream) -> float:
 
 
 def gemm_kernel_times(wl: Workload, stream, launches: int = 60, reps: int = 5) -> list[float]:
-    """Average duration (s) of one fp8_block_gemm launch per shape: a CUDA
-    graph of `launches` back-to-back calls over the rotating weight copies,
-    timed with events on the launching stream, median over `reps` replays."""
-    from block_scaled_fp8_act_gb300 import fp8act
+    """Average duration (s) of one GEMM launch per shape: a CUDA graph of
+    `launches` back-to-back calls over the rotating weight copies, timed with
+    events on the launching stream, median over `reps` replays."""
     out = []
     for si in range(len(wl.shapes)):
         def chain(si=si):
             for i in range(launches):
-                c = i % wl.copies
-                fp8act.fp8_block_gemm(wl.q[si], wl.sa[si], wl.w[si][c], wl.sw[si][c], wl.out[si], stream=stream)
+                wl.gemm(si, i % wl.copies, stream)
         g = capture(chain, stream)
         ts = []
         for _ in range(reps):
@@ -403,11 +426,14 @@ def main() -> None:
     desc = WORKLOADS[args.workload][1].format(M=M, k=M - 1)
     # FP8 ridge point ~560 flop/B (measured tensor / HBM peaks) ~ M = 280 tokens
     bound = "tensor" if M > 280 else "hbm"
+    weight_only = args.workload in WEIGHT_ONLY
+    if weight_only and M > 16:
+        ap.error("the weight-only workload is a decode path (M <= 16)")
     kernel = gemm_kernel_name(M)
     weights = Weights(device)
-    wl = Workload(M, weights, device)
+    wl = Workload(M, weights, device, weight_only=weight_only)
     graphs = [capture(lambda c=c: wl.enqueue_step(c, stream), stream) for c in range(wl.copies)]
-    launches_per_step = 2 * len(wl.shapes)
+    launches_per_step = wl.launches_per_step()
 
     # ---- timed region: K steps of the whole path, graphs replayed back to back
     for i in range(args.warmup):
@@ -461,7 +487,7 @@ def main() -> None:
     h2d = sum(x.numel() * 2 for x in wl.x_host)
     d2h = sum(o.numel() * 2 for o in wl.out_host)
 
-    gemm_bytes = [algorithmic_gemm_bytes(M, N, K) for N, K in wl.shapes]
+    gemm_bytes = [wl.gemm_bytes_of(N, K) for N, K in wl.shapes]
     gemm_flops = [2.0 * M * N * K for N, K in wl.shapes]
     traffic = recorded_traffic(kernel, f"{args.workload}_m{M}_mean_of_5")
     if bound == "tensor":
@@ -490,11 +516,13 @@ def main() -> None:
         "metric": METRIC if args.workload == "decode" else f"block-FP8 linear, {desc}",
         "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 acc -> bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 x e4m3 -> f32 acc -> bf16" if weight_only else "e4m3 x e4m3 -> f32 acc -> bf16",
+        "data": "synthetic",
         "config": {"workload": desc, "M": M, "shapes": [list(s) for s in wl.shapes],
                    "l2": f"inputs larger than L2: {wl.copies} rotating weight copies "
                          f"({wl.copies * sum(N * K for N, K in wl.shapes) / 1e6:.0f} MB), no flush",
-                   "graphs": "each step is one CUDA graph replay (10 kernels)",
+                   "graphs": f"each step is one CUDA graph replay ({launches_per_step} kernels)",
                    "parallelism": f"replicas x{world}"},
         "us_per_call": per_shape,
         "gpu_launches": args.steps * launches_per_step,
@@ -507,7 +535,7 @@ def main() -> None:
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 5)},
         "clocks": clk.summary(),
     }
-    if not args.no_sweep and rank == 0:
+    if not args.no_sweep and rank == 0 and not weight_only:
         del wl
         torch.cuda.empty_cache()
         result["sweep"] = sweep(weights, device, stream, peaks)

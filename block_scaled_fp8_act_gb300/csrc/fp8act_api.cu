@@ -68,6 +68,20 @@ int gemm_common(const void* q, const float* sa, const void* w, const float* sw, 
     return launch_status(fp8act::launch_gemm_tc(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
 }
 
+int w8a16_common(const void* x, const void* w, const float* sw, int M, int N, int K, void* out, bool out_f32,
+                 void* stream) {
+    if (M < 0 || N < 0) return FP8ACT_ERR_SHAPE;
+    if (int st = check_k(K)) return st;
+    if (M == 0 || N == 0) return FP8ACT_OK;
+    if (!x || !w || !sw || !out) return FP8ACT_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(out, 16) || !aligned(sw, 4)) return FP8ACT_ERR_ALIGN;
+    int st = FP8ACT_OK;
+    const int sms = current_device_sms(&st);
+    if (st) return st;
+    return launch_status(fp8act::launch_gemm_w8a16(x, static_cast<const uint8_t*>(w), sw, M, N, K, out, out_f32, sms,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -104,6 +118,16 @@ int fp8_block_gemm(const void* q_e4m3, const float* sa, const void* w_e4m3, cons
 int fp8_block_gemm_f32(const void* q_e4m3, const float* sa, const void* w_e4m3, const float* sw, int M, int N,
                        int K, float* out_f32, void* stream) {
     return gemm_common(q_e4m3, sa, w_e4m3, sw, M, N, K, out_f32, true, stream);
+}
+
+int fp8_block_gemm_w8a16(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N, int K,
+                         void* out_bf16, void* stream) {
+    return w8a16_common(x_bf16, w_e4m3, sw, M, N, K, out_bf16, false, stream);
+}
+
+int fp8_block_gemm_w8a16_f32(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N, int K,
+                             float* out_f32, void* stream) {
+    return w8a16_common(x_bf16, w_e4m3, sw, M, N, K, out_f32, true, stream);
 }
 
 const char* fp8act_strerror(int status) {

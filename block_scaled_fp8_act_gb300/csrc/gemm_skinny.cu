@@ -33,7 +33,18 @@
 //    by sa[m, kb] * sw[n/128, kb] and added into the warp's running sums.
 //  - The warps' partial sums meet in shared memory and one pass writes the
 //    16 x M outputs (bf16, or fp32 for the error-analysis entry point).
+//
+// Weight-only mode (kA16): the activations stay bf16 (no quantisation
+// launch, the job of the weight-only FP8 back-end that the same post uses at
+// one request, section "单并发优化"). Each lane widens its 32 weight codes of
+// a block to bf16 (E4M3 -> f16 -> f32 -> bf16, exact at every step) and runs
+// eight m16n8k16 bf16 MMAs per block, with the same K permutation: MMA i
+// takes codes 4i..4i+3 of the lane's 32 and the lane's activations at the
+// same positions (64 bytes of bf16 per lane and block). Only the weight
+// scale multiplies the block's dot.
 #include <atomic>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -53,9 +64,41 @@ __device__ __forceinline__ void mma_e4m3_16x8x32(float (&d)[4], uint32_t a0, uin
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 codes (code 0 in the low byte) -> bf16x2 (value 0 in the low
+// half). Every E4M3 value, subnormals included, is a normal f16 and a normal
+// bf16, so each conversion step is exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(codes & 0xFFFFu)));
+    __half2 h;
+    memcpy(&h, &h2, 4);
+    const float2 f = __half22float2(h);
+    return pack_bf16x2(f.x, f.y);
+}
+
+// Eight weight words (32 codes, in the lane's K order) -> sixteen bf16x2 words.
+__device__ __forceinline__ void widen_row(const uint4& lo, const uint4& hi, uint32_t (&r)[16]) {
+    const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        r[2 * i] = e4m3x2_to_bf16x2(wd[i]);
+        r[2 * i + 1] = e4m3x2_to_bf16x2(wd[i] >> 16);
+    }
+}
+
 // kUnroll = K blocks whose weight loads a warp has in flight at once;
-// kTG = groups of 8 tokens a CTA handles (they share the weight fragments).
-template <bool kF32Out, int kUnroll, int kTG>
+// kTG = groups of 8 tokens a CTA handles (they share the weight fragments);
+// kA16 = bf16 activations in `q` (weight-only mode; `sa` unused).
+template <bool kF32Out, int kUnroll, int kTG, bool kA16 = false>
 __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
     const uint8_t* __restrict__ q, const float* __restrict__ sa, const uint8_t* __restrict__ w,
     const float* __restrict__ sw, int M, int N, int K, void* __restrict__ out) {
@@ -101,6 +144,43 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
         if (!waited) {
             ptx::griddep_wait();
             waited = true;
+        }
+        if constexpr (kA16) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int kb = kb0 + u * nwarps;
+                if (kb >= KB) continue;
+                uint32_t wa[16], wb[16];  // rows g and g + 8, bf16x2
+                widen_row(r0lo[u], r0hi[u], wa);
+                widen_row(r1lo[u], r1hi[u], wb);
+                const float s_w = __ldg(sw_r + kb);
+                const int64_t off = static_cast<int64_t>(kb) * kGroup * 2;
+#pragma unroll
+                for (int j = 0; j < kTG; ++j) {
+                    const int m = m0 + 8 * j + g;
+                    const bool ok_x = m < M;
+                    const uint8_t* x_r = q + (static_cast<int64_t>(m) * K + 16 * t) * 2 + off;
+                    const uint4 x0 = ok_x ? ld_shared_ro_v4(x_r) : zero;
+                    const uint4 x1 = ok_x ? ld_shared_ro_v4(x_r + 16) : zero;
+                    const uint4 x2 = ok_x ? ld_shared_ro_v4(x_r + 128) : zero;
+                    const uint4 x3 = ok_x ? ld_shared_ro_v4(x_r + 144) : zero;
+                    const uint32_t xw[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                             x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        mma_bf16_16x8x16(d, wa[2 * i], wb[2 * i], wa[2 * i + 1], wb[2 * i + 1], xw[2 * i],
+                                         xw[2 * i + 1]);
+                    const int c0 = m0 + 8 * j + 2 * t;
+                    const float s0 = c0 < M ? s_w : 0.f;
+                    const float s1 = c0 + 1 < M ? s_w : 0.f;
+                    acc[j][0] = fmaf(d[0], s0, acc[j][0]);
+                    acc[j][1] = fmaf(d[1], s1, acc[j][1]);
+                    acc[j][2] = fmaf(d[2], s0, acc[j][2]);
+                    acc[j][3] = fmaf(d[3], s1, acc[j][3]);
+                }
+            }
+            continue;
         }
 #pragma unroll
         for (int j = 0; j < kTG; ++j) {
@@ -166,7 +246,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
 
 // CTAs per SM for a (load depth, token groups, warps) configuration, from the
 // occupancy API, cached per device.
-template <bool kF32Out, int kUnroll, int kTG>
+template <bool kF32Out, int kUnroll, int kTG, bool kA16>
 int ctas_per_sm(int wv) {
     static std::atomic<int> cache[64][kMaxWarps + 1];  // 0 = unknown, else 1 + CTAs per SM
     int dev = 0;
@@ -174,8 +254,8 @@ int ctas_per_sm(int wv) {
     int cached = cache[dev & 63][wv].load(std::memory_order_relaxed);
     if (cached == 0) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out, kUnroll, kTG>, 32 * wv,
-                                                          0) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out, kUnroll, kTG, kA16>,
+                                                          32 * wv, 0) != cudaSuccess) {
             cudaGetLastError();
             per_sm = 0;
         }
@@ -189,7 +269,7 @@ int ctas_per_sm(int wv) {
 // evenly to within 10% (every warp finishes at about the same time) and for
 // which the whole grid is resident in one wave, the one with the most weight
 // bytes in flight (capped where HBM saturates, ~20 MB on GB300); 0 if none.
-template <bool kF32Out, int kUnroll, int kTG>
+template <bool kF32Out, int kUnroll, int kTG, bool kA16 = false>
 int pick_warps(int64_t ctas, int KB, int num_sms, int64_t* inflight_out) {
     constexpr int64_t kSaturate = int64_t(20) << 20;
     int best = 0;
@@ -197,7 +277,7 @@ int pick_warps(int64_t ctas, int KB, int num_sms, int64_t* inflight_out) {
     for (int wv = 1; wv <= kMaxWarps && wv <= KB; ++wv) {
         const int per_warp = (KB + wv - 1) / wv;
         if (10 * KB < 9 * wv * per_warp) continue;  // warps would finish more than 10% apart
-        if (ctas > static_cast<int64_t>(ctas_per_sm<kF32Out, kUnroll, kTG>(wv)) * num_sms) continue;
+        if (ctas > static_cast<int64_t>(ctas_per_sm<kF32Out, kUnroll, kTG, kA16>(wv)) * num_sms) continue;
         int64_t inflight = ctas * wv * (per_warp < kUnroll ? per_warp : kUnroll) * (16 * kGroup);
         if (inflight > kSaturate) inflight = kSaturate;
         if (inflight > best_inflight || (inflight == best_inflight && wv < best)) {
@@ -209,7 +289,7 @@ int pick_warps(int64_t ctas, int KB, int num_sms, int64_t* inflight_out) {
     return best;
 }
 
-template <bool kF32Out, int kUnroll, int kTG>
+template <bool kF32Out, int kUnroll, int kTG, bool kA16 = false>
 cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N, int K,
                          void* out, int num_sms, cudaStream_t stream) {
     const int KB = K / kGroup;
@@ -217,7 +297,7 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
     const int64_t ctas = static_cast<int64_t>(grid.x) * grid.y;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    int wv = pick_warps<kF32Out, kUnroll, kTG>(ctas, KB, num_sms, nullptr);
+    int wv = pick_warps<kF32Out, kUnroll, kTG, kA16>(ctas, KB, num_sms, nullptr);
     if (wv == 0) wv = KB < 4 ? KB : 4;  // grid larger than one wave: plain 4-warp CTAs
     cfg.blockDim = dim3(32 * wv);
     cfg.stream = stream;
@@ -226,7 +306,7 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<kF32Out, kUnroll, kTG>, q, sa, w, sw, M, N, K, out);
+    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<kF32Out, kUnroll, kTG, kA16>, q, sa, w, sw, M, N, K, out);
 }
 
 }  // namespace
@@ -264,6 +344,16 @@ cudaError_t launch_gemm_skinny(const uint8_t* q, const float* sa, const uint8_t*
         if (KB >= 32 && in4 > in2) unroll = 4;
     }
     return launch_gemm_skinny_unroll(q, sa, w, sw, M, N, K, out, out_f32, num_sms, unroll, stream);
+}
+
+cudaError_t launch_gemm_w8a16(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
+                              bool out_f32, int num_sms, cudaStream_t stream) {
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    if (M > 8)  // two token groups per CTA share the widened weights
+        return out_f32 ? launch_typed<true, 2, 2, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
+                       : launch_typed<false, 2, 2, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
+    return out_f32 ? launch_typed<true, 2, 1, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
+                   : launch_typed<false, 2, 1, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
 }
 
 }  // namespace fp8act

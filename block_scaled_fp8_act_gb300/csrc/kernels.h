@@ -25,6 +25,11 @@ cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const u
                                       int N, int K, void* out, bool out_f32, int num_sms, int unroll,
                                       cudaStream_t stream);
 
+// Weight-only variant of the same kernel: bf16 activations x [M, K], no
+// activation scales (E4M3 weights widened to bf16, bf16 MMAs).
+cudaError_t launch_gemm_w8a16(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
+                              bool out_f32, int num_sms, cudaStream_t stream);
+
 // Tensor-memory (tcgen05) GEMM: 128 x 256 (prefill) or 128 x 128 output
 // tiles, TMA-fed ring, per-K-group promotion of the fp32 block scales in the
 // epilogue, split K over a thread-block cluster when the tiles are too few.

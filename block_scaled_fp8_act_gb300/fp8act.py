@@ -53,10 +53,13 @@ def load(build: bool = False) -> ctypes.CDLL:
     L.fp8_weight_quant.argtypes = [p, i, i, p, p, p]
     L.fp8_block_gemm.argtypes = [p, p, p, p, i, i, i, p, p]
     L.fp8_block_gemm_f32.argtypes = [p, p, p, p, i, i, i, p, p]
+    L.fp8_block_gemm_w8a16.argtypes = [p, p, p, i, i, i, p, p]
+    L.fp8_block_gemm_w8a16_f32.argtypes = [p, p, p, i, i, i, p, p]
     L.fp8act_strerror.argtypes = [i]
     L.fp8act_strerror.restype = ctypes.c_char_p
     L.fp8act_check_status.argtypes = [p]
     for fn in (L.fp8_act_quant, L.fp8_weight_quant, L.fp8_block_gemm, L.fp8_block_gemm_f32,
+               L.fp8_block_gemm_w8a16, L.fp8_block_gemm_w8a16_f32,
                L.fp8act_check_status, L.fp8act_version):
         fn.restype = ctypes.c_int
     _lib = L
@@ -145,6 +148,33 @@ def fp8_block_gemm(q, sa, w, sw, out=None, stream=None) -> torch.Tensor:
 def fp8_block_gemm_f32(q, sa, w, sw, out=None, stream=None) -> torch.Tensor:
     """fp32 [M, N] output of the same kernels (no bf16 cast)."""
     return _gemm("fp8_block_gemm_f32", torch.float32, q, sa, w, sw, out, stream)
+
+
+def _gemm_w8a16(fn_name: str, out_dtype, x, w, sw, out, stream):
+    _cuda2d(x, (torch.bfloat16,), "x")
+    _cuda2d(w, _CODES, "w")
+    _cuda2d(sw, (torch.float32,), "sw")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or sw.shape != ((N + G - 1) // G, K // G):
+        raise ValueError("inconsistent x / w / sw shapes")
+    out = torch.empty((M, N), dtype=out_dtype, device=x.device) if out is None else out
+    _cuda2d(out, (out_dtype,), "out")
+    if out.shape != (M, N):
+        raise ValueError("out has the wrong shape")
+    fn = getattr(load(), fn_name)
+    _check(fn_name, fn(x.data_ptr(), w.data_ptr(), sw.data_ptr(), M, N, K, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def fp8_block_gemm_w8a16(x, w, sw, out=None, stream=None) -> torch.Tensor:
+    """bf16 [M, N] = bf16 x [M, K] times block-scaled E4M3 w [N, K]^T (no activation quantisation)."""
+    return _gemm_w8a16("fp8_block_gemm_w8a16", torch.bfloat16, x, w, sw, out, stream)
+
+
+def fp8_block_gemm_w8a16_f32(x, w, sw, out=None, stream=None) -> torch.Tensor:
+    """fp32 [M, N] output of the weight-only kernels (no bf16 cast)."""
+    return _gemm_w8a16("fp8_block_gemm_w8a16_f32", torch.float32, x, w, sw, out, stream)
 
 
 def check_status(stream=None) -> int:

@@ -101,6 +101,27 @@ FP8ACT_API int fp8_block_gemm(const void* q_e4m3, const float* sa, const void* w
 FP8ACT_API int fp8_block_gemm_f32(const void* q_e4m3, const float* sa, const void* w_e4m3, const float* sw,
                        int M, int N, int K, float* out_f32, void* stream);
 
+/*
+ * Weight-only block-FP8 GEMM (W8A16): the bf16 activations times the same
+ * block-scaled E4M3 weights, with no activation quantisation:
+ *   out[m, n] = bf16( sum_kb sw[n/128, kb] * sum_{k in block kb} x[m, k] * w[n, k] ),
+ * each E4M3 weight widened exactly to bf16, bf16 x bf16 products, fp32
+ * accumulation. This is the role of the weight-only FP8 back-end (Marlin)
+ * that "单并发提速73%,多并发能力达原来2.4倍:Qwen3.8-27B性能优化实践"
+ * (smartx.com), section "单并发优化", picks at one request: it saves the
+ * quantisation launch per linear layer. The kernel is the weight-streaming
+ * one of fp8_block_gemm; it reads the weights once per 16 tokens, so it is
+ * meant for decode (M <= 16). Every M >= 1 is supported.
+ *   x_bf16     : [M, K] bf16 activations (16-byte aligned)
+ *   w_e4m3, sw : weight codes [N, K] and scales [ceil(N/128), K/128]
+ *   out_bf16   : [M, N] bf16 out (out_f32: [M, N] fp32, the value before the cast)
+ * Errors as for fp8_block_gemm.
+ */
+FP8ACT_API int fp8_block_gemm_w8a16(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N, int K,
+                                    void* out_bf16, void* stream);
+FP8ACT_API int fp8_block_gemm_w8a16_f32(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N,
+                                        int K, float* out_f32, void* stream);
+
 /* A static English description of a status code (never NULL). */
 FP8ACT_API const char* fp8act_strerror(int status);
 

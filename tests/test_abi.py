@@ -21,6 +21,7 @@ def lib():
 def test_library_exports_every_header_symbol(lib):
     names = fp8act.header_symbols()
     assert {"fp8_act_quant", "fp8_weight_quant", "fp8_block_gemm", "fp8_block_gemm_f32",
+            "fp8_block_gemm_w8a16", "fp8_block_gemm_w8a16_f32",
             "fp8act_strerror", "fp8act_check_status", "fp8act_version"} <= set(names)
     raw = ctypes.CDLL(fp8act.lib_path())
     for n in names:
@@ -78,3 +79,15 @@ def test_valid_call_without_a_gb300_is_refused(lib):
         pytest.skip("a GPU is present; covered by the GPU tests")
     assert lib.fp8_block_gemm(A16, A16, A16, A16, 1, 128, 128, A16, None) == DEVICE
     assert lib.fp8_act_quant(A16, 1, 128, A16, A16, None) == DEVICE
+
+
+@pytest.mark.parametrize("name", ["fp8_block_gemm_w8a16", "fp8_block_gemm_w8a16_f32"])
+def test_w8a16_argument_checks(lib, name):
+    f = getattr(lib, name)
+    assert f(A16, A16, A16, 1, 128, 64, A16, None) == SHAPE
+    assert f(A16, A16, A16, -1, 128, 128, A16, None) == SHAPE
+    assert f(None, None, None, 0, 128, 128, None, None) == OK
+    assert f(A16, None, A16, 1, 128, 128, A16, None) == NULL
+    assert f(A16 + 8, A16, A16, 1, 128, 128, A16, None) == ALIGN
+    assert f(A16, A16, A16 + 2, 1, 128, 128, A16, None) == ALIGN
+    assert f(A16, A16, A16, 1, 128, 128, A16 + 4, None) == ALIGN

@@ -182,3 +182,44 @@ def test_gemm_writes_nothing_outside_out(fp8act):
 
 def test_status_is_clean(fp8act):
     assert fp8act.check_status() == 0
+
+
+# ------------------------------------------------------- weight-only (W8A16)
+def _w8a16_compare(fp8act, p, M, seed, rows=None):
+    from parity_util import compare_gemm
+    x = inputs.activations_bf16(M, p.K, seed)
+    xd = x.cuda()
+    out = fp8act.fp8_block_gemm_w8a16(xd, p.w, p.sw)
+    out32 = fp8act.fp8_block_gemm_w8a16_f32(xd, p.w, p.sw)
+    torch.cuda.synchronize()
+    y, aabs, ref = oracle.block_gemm_w8a16(inputs.bf16_bits(x), p.w_ref, p.sw_ref, rows=rows)
+    if rows is not None:
+        idx = torch.as_tensor(np.asarray(rows), device=out.device)
+        out, out32 = out.index_select(0, idx), out32.index_select(0, idx)
+    return compare_gemm(out, out32, y, aabs, ref, p.K)
+
+
+@pytest.mark.parametrize("si", range(len(SHAPES)))
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 12, 16])
+def test_w8a16_decode_widths(fp8act, si, M):
+    _w8a16_compare(fp8act, problem(si), M, seed=500 + M)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 17, 128), (5, 200, 256), (12, 1000, 384), (40, 257, 768)])
+def test_w8a16_ragged(fp8act, M, N, K):
+    from parity_util import Problem
+    _w8a16_compare(fp8act, Problem(N, K, seed=N + 3 * K), M, seed=M)
+
+
+def test_w8a16_edge_activations_and_determinism(fp8act):
+    from parity_util import compare_gemm
+    p = problem(1)
+    x = inputs.edge_activations_bf16(7, p.K, seed=9)
+    xd = x.cuda()
+    a = fp8act.fp8_block_gemm_w8a16_f32(xd, p.w, p.sw)
+    b = fp8act.fp8_block_gemm_w8a16_f32(xd, p.w, p.sw)
+    out = fp8act.fp8_block_gemm_w8a16(xd, p.w, p.sw)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    y, aabs, ref = oracle.block_gemm_w8a16(inputs.bf16_bits(x), p.w_ref, p.sw_ref)
+    compare_gemm(out, a, y, aabs, ref, p.K)
