@@ -314,46 +314,45 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
 cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
                                       int N, int K, void* out, bool out_f32, int num_sms, int unroll,
                                       cudaStream_t stream) {
-    if (M > 8)  // two token groups per CTA: the weight fragments serve 16 tokens
-        return out_f32 ? launch_typed<true, 2, 2>(q, sa, w, sw, M, N, K, out, num_sms, stream)
-                       : launch_typed<false, 2, 2>(q, sa, w, sw, M, N, K, out, num_sms, stream);
+    // Above M = 8 the grid gets one row of CTAs per 8 tokens (each re-reads
+    // the weights, mostly from L2); for 9..16 tokens this measured faster than
+    // CTAs that hold 16 tokens against one weight fragment.
     if (unroll >= 4)
         return out_f32 ? launch_typed<true, 4, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream)
                        : launch_typed<false, 4, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream);
-    return out_f32 ? launch_typed<true, 2, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream)
-                   : launch_typed<false, 2, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream);
+    if (unroll >= 2)
+        return out_f32 ? launch_typed<true, 2, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream)
+                       : launch_typed<false, 2, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream);
+    return out_f32 ? launch_typed<true, 1, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream)
+                   : launch_typed<false, 1, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream);
 }
 
 cudaError_t launch_gemm_skinny(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
                                int N, int K, void* out, bool out_f32, int num_sms, cudaStream_t stream) {
-    // Load depth: 4 K groups in flight per warp (128 registers, fewer warps)
-    // when that puts more bytes in flight than depth 2; short K (< 32 groups)
-    // keeps depth 2, which measured faster there (more, shorter warps).
-    int unroll = 2;
-    if (M <= 8) {
-        const int KB = K / kGroup;
-        const int64_t ctas = (N + 15) / 16;
-        int64_t in2 = 0, in4 = 0;
-        if (out_f32) {
-            pick_warps<true, 2, 1>(ctas, KB, num_sms, &in2);
-            pick_warps<true, 4, 1>(ctas, KB, num_sms, &in4);
-        } else {
-            pick_warps<false, 2, 1>(ctas, KB, num_sms, &in2);
-            pick_warps<false, 4, 1>(ctas, KB, num_sms, &in4);
-        }
-        if (KB >= 32 && in4 > in2) unroll = 4;
-    }
+    // Load depth per warp step. Long K (>= 32 blocks): one block per step,
+    // which takes the fewest registers (64) and so leaves room for the most
+    // warps while the whole grid stays resident; it measured fastest on every
+    // long-K projection at M = 1..16. Short K: four blocks per step; the loop
+    // is only a few steps long, so most of each warp's weights are requested
+    // before the programmatic-launch wait and overlap the previous kernel.
+    const int KB = K / kGroup;
+    const int unroll = KB >= 32 ? 1 : 4;
     return launch_gemm_skinny_unroll(q, sa, w, sw, M, N, K, out, out_f32, num_sms, unroll, stream);
 }
 
 cudaError_t launch_gemm_w8a16(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
                               bool out_f32, int num_sms, cudaStream_t stream) {
+    // One K block per warp step: the widened weights and the bf16
+    // activations make each block in flight cost more registers than in the
+    // W8A8 mode, and with the whole grid resident in one wave the register
+    // count per thread sets how many warps (and so how many weight bytes)
+    // each SM keeps in flight. Depth 1 measured fastest at M = 1, 8 and 16.
     const uint8_t* xb = static_cast<const uint8_t*>(x);
     if (M > 8)  // two token groups per CTA share the widened weights
-        return out_f32 ? launch_typed<true, 2, 2, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
-                       : launch_typed<false, 2, 2, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
-    return out_f32 ? launch_typed<true, 2, 1, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
-                   : launch_typed<false, 2, 1, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
+        return out_f32 ? launch_typed<true, 1, 2, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
+                       : launch_typed<false, 1, 2, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
+    return out_f32 ? launch_typed<true, 1, 1, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
+                   : launch_typed<false, 1, 1, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
 }
 
 }  // namespace fp8act

@@ -16,11 +16,11 @@ cudaError_t launch_weight_quant(const void* W, int64_t N, int64_t K, void* w, fl
 
 // Weight-streaming GEMM for small M (tensor-core mma.sync, 16-row tiles,
 // K split across the warps of a CTA, programmatic dependent launch). Any M
-// works (tokens in groups of 16 above M = 8) but it re-reads the weights
-// once per group, so it is the M <= 16 path.
+// works (one row of CTAs per 8 tokens) but every row re-reads the weights,
+// so it is the M <= 16 path.
 cudaError_t launch_gemm_skinny(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
                                int N, int K, void* out, bool out_f32, int num_sms, cudaStream_t stream);
-// The same with an explicit load depth per warp (2 or 4 K blocks in flight).
+// The same with an explicit load depth per warp (1, 2 or 4 K blocks per step).
 cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
                                       int N, int K, void* out, bool out_f32, int num_sms, int unroll,
                                       cudaStream_t stream);
