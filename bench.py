@@ -21,7 +21,8 @@ Printed JSON line (rank 0):
 
 `--workload verify|batched|prefill` times the same step at M = 8, 102 or
 4096; `--workload decode-w8a16` times the weight-only variant at M = 1 (bf16
-activations straight into the GEMM, no quantisation launch).
+activations straight into the GEMM, no quantisation launch); `--workload
+lmhead` times one vocabulary-sized head (N = 151936, K = 5120) at M = 1.
 `--impl reference` times the CPU oracle instead (the reference arm).
 """
 from __future__ import annotations
@@ -59,7 +60,10 @@ WORKLOADS = {
                       "(act quant + block-FP8 GEMM per shape)", "tensor"),
     "decode-w8a16": (1, "weight-only decode M={M} over the five dense-27B projection shapes "
                         "(bf16 activations x block-FP8 weights, one GEMM per shape, no act quant)", "hbm"),
+    "lmhead": (1, "vocabulary-sized head M={M}: N=151936, K=5120 (act quant + block-FP8 GEMM)", "hbm"),
 }
+# Workloads on other shapes than the five projections: (shapes, weight seed indices).
+WORKLOAD_SHAPES = {"lmhead": ((inputs.VOCAB_SHAPE,), (inputs.VOCAB_SEED_INDEX,))}
 WEIGHT_ONLY = {"decode-w8a16"}
 
 
@@ -187,13 +191,14 @@ class Weights:
     """E4M3 weights + scales of the five shapes in `copies` rotating copies
     (quantised on the device by fp8_weight_quant)."""
 
-    def __init__(self, device: torch.device, copies: int = WEIGHT_COPIES, shapes=inputs.SHAPES):
+    def __init__(self, device: torch.device, copies: int = WEIGHT_COPIES, shapes=inputs.SHAPES, seed_index=None):
         from block_scaled_fp8_act_gb300 import fp8act
         self.shapes = list(shapes)
         self.copies = copies
+        self.seed_index = list(seed_index) if seed_index is not None else list(range(len(self.shapes)))
         self.w, self.sw = [], []
         for si, (N, K) in enumerate(self.shapes):
-            W = inputs.weights_bf16(N, K, inputs.weight_seed(si)).to(device)
+            W = inputs.weights_bf16(N, K, inputs.weight_seed(self.seed_index[si])).to(device)
             w0, sw0 = fp8act.fp8_weight_quant(W)
             del W
             self.w.append([w0] + [w0.clone() for _ in range(copies - 1)])
@@ -430,7 +435,11 @@ def main() -> None:
     if weight_only and M > 16:
         ap.error("the weight-only workload is a decode path (M <= 16)")
     kernel = gemm_kernel_name(M)
-    weights = Weights(device)
+    if args.workload in WORKLOAD_SHAPES:
+        shapes, seeds = WORKLOAD_SHAPES[args.workload]
+        weights = Weights(device, shapes=shapes, seed_index=seeds)
+    else:
+        weights = Weights(device)
     wl = Workload(M, weights, device, weight_only=weight_only)
     graphs = [capture(lambda c=c: wl.enqueue_step(c, stream), stream) for c in range(wl.copies)]
     launches_per_step = wl.launches_per_step()
@@ -535,7 +544,7 @@ def main() -> None:
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 5)},
         "clocks": clk.summary(),
     }
-    if not args.no_sweep and rank == 0 and not weight_only:
+    if not args.no_sweep and rank == 0 and not weight_only and args.workload not in WORKLOAD_SHAPES:
         del wl
         torch.cuda.empty_cache()
         result["sweep"] = sweep(weights, device, stream, peaks)

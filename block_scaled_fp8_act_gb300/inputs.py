@@ -35,6 +35,14 @@ SHAPES: tuple[tuple[int, int], ...] = (
     (8192, 5120),
 )
 
+#: (N, K) of a vocabulary-sized head (the draft / LM head that reads the whole
+#: vocabulary every decode step, single-RTX-PRO-6000 Qwen3.8-27B post, section
+#: "单并发优化"). The pages give no vocabulary size; 151936 (1187 blocks of 128)
+#: is the vocabulary of the model family, K = 5120 its hidden size.
+VOCAB_SHAPE: tuple[int, int] = (151936, 5120)
+#: Seed index of the vocabulary head's weights (after the five projections).
+VOCAB_SEED_INDEX = len(SHAPES)
+
 #: Token counts per call: decode, speculative verify, batched decode, prefill.
 M_DECODE = (1,)
 M_VERIFY = (2, 3, 4, 5, 6, 7, 8)

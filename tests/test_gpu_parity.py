@@ -223,3 +223,24 @@ def test_w8a16_edge_activations_and_determinism(fp8act):
     assert torch.equal(a, b)
     y, aabs, ref = oracle.block_gemm_w8a16(inputs.bf16_bits(x), p.w_ref, p.sw_ref)
     compare_gemm(out, a, y, aabs, ref, p.K)
+
+
+# ------------------------------------------------- vocabulary-sized head GEMV
+@pytest.fixture(scope="module")
+def vocab_problem(fp8act):
+    from parity_util import Problem
+    N, K = inputs.VOCAB_SHAPE
+    p = Problem(N, K, inputs.weight_seed(inputs.VOCAB_SEED_INDEX))
+    assert np.array_equal(p.w.cpu().numpy(), p.w_ref) and np.array_equal(p.sw.cpu().numpy(), p.sw_ref)
+    return p
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_vocab_head_gemv(fp8act, vocab_problem, M):
+    """N = 151936 gives a grid of 9496 CTAs, far more than one wave: the
+    multi-wave launch path of the weight-streaming kernel."""
+    vocab_problem.run_and_compare(M, seed=700 + M)
+
+
+def test_vocab_head_w8a16(fp8act, vocab_problem):
+    _w8a16_compare(fp8act, vocab_problem, 1, seed=711)
