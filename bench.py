@@ -23,6 +23,8 @@ Printed JSON line (rank 0):
 4096; `--workload decode-w8a16` times the weight-only variant at M = 1 (bf16
 activations straight into the GEMM, no quantisation launch); `--workload
 lmhead` times one vocabulary-sized head (N = 151936, K = 5120) at M = 1.
+`--workload decode-grouped` runs the five projections as independent problems
+of one grouped act-quant launch and one grouped GEMM launch.
 `--impl reference` times the CPU oracle instead (the reference arm).
 """
 from __future__ import annotations
@@ -61,7 +63,10 @@ WORKLOADS = {
     "decode-w8a16": (1, "weight-only decode M={M} over the five dense-27B projection shapes "
                         "(bf16 activations x block-FP8 weights, one GEMM per shape, no act quant)", "hbm"),
     "lmhead": (1, "vocabulary-sized head M={M}: N=151936, K=5120 (act quant + block-FP8 GEMM)", "hbm"),
+    "decode-grouped": (1, "grouped decode M={M}: the five dense-27B projection shapes as independent problems, "
+                          "one grouped act-quant launch + one grouped block-FP8 GEMM launch", "hbm"),
 }
+GROUPED = {"decode-grouped"}
 # Workloads on other shapes than the five projections: (shapes, weight seed indices).
 WORKLOAD_SHAPES = {"lmhead": ((inputs.VOCAB_SHAPE,), (inputs.VOCAB_SEED_INDEX,))}
 WEIGHT_ONLY = {"decode-w8a16"}
@@ -105,6 +110,7 @@ def load_peaks() -> tuple[dict, str]:
 
 KERNEL_SOURCES = {
     "gemm_skinny_kernel": ("gemm_skinny.cu", "common.cuh", "sm100_ptx.cuh"),
+    "gemm_skinny_grouped_kernel": ("gemm_skinny.cu", "common.cuh", "sm100_ptx.cuh"),
     "gemm_tc_kernel": ("gemm_tc.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
 }
 
@@ -210,9 +216,11 @@ class Workload:
     """Device-resident activations of one M over the five shapes (plus pinned
     host copies for the end-to-end leg), sharing one Weights set."""
 
-    def __init__(self, M: int, weights: Weights, device: torch.device, weight_only: bool = False):
+    def __init__(self, M: int, weights: Weights, device: torch.device, weight_only: bool = False,
+                 grouped: bool = False):
         self.M = M
         self.weight_only = weight_only
+        self.grouped = grouped
         self.shapes = weights.shapes
         self.copies = weights.copies
         self.w, self.sw = weights.w, weights.sw
@@ -236,7 +244,22 @@ class Workload:
                    for N, K in self.shapes)
 
     def launches_per_step(self) -> int:
+        if self.grouped:
+            return 2
         return (1 if self.weight_only else 2) * len(self.shapes)
+
+    def gemm_units(self) -> list:
+        """The GEMM launches of one step: (label, algorithmic bytes, flops, enqueue(copy, stream))."""
+        if self.grouped:
+            return [("all five, grouped", sum(self.gemm_bytes_of(N, K) for N, K in self.shapes),
+                     sum(2.0 * self.M * N * K for N, K in self.shapes), self.gemm_grouped)]
+        return [((N, K), self.gemm_bytes_of(N, K), 2.0 * self.M * N * K,
+                 lambda c, s, si=si: self.gemm(si, c, s)) for si, (N, K) in enumerate(self.shapes)]
+
+    def gemm_grouped(self, copy: int, stream) -> None:
+        from block_scaled_fp8_act_gb300 import fp8act
+        fp8act.fp8_block_gemm_grouped([(self.q[si], self.sa[si], self.w[si][copy], self.sw[si][copy])
+                                       for si in range(len(self.shapes))], outs=self.out, stream=stream)
 
     def gemm(self, si: int, copy: int, stream) -> None:
         from block_scaled_fp8_act_gb300 import fp8act
@@ -249,10 +272,18 @@ class Workload:
 
     def enqueue_step(self, copy: int, stream) -> None:
         from block_scaled_fp8_act_gb300 import fp8act
+        if self.grouped:
+            fp8act.fp8_act_quant_grouped(self.x, outs=list(zip(self.q, self.sa)), stream=stream)
+            self.gemm_grouped(copy, stream)
+            return
         for si in range(len(self.shapes)):
             if not self.weight_only:
                 fp8act.fp8_act_quant(self.x[si], self.q[si], self.sa[si], stream=stream)
             self.gemm(si, copy, stream)
+
+
+def _label(lb) -> dict:
+    return {"N": lb[0], "K": lb[1]} if isinstance(lb, tuple) else {"launch": lb}
 
 
 def capture(fn, stream) -> torch.cuda.CUDAGraph:
@@ -281,14 +312,15 @@ def time_graphs(graphs, steps: int, warmup: int, stream) -> float:
 
 
 def gemm_kernel_times(wl: Workload, stream, launches: int = 60, reps: int = 5) -> list[float]:
-    """Average duration (s) of one GEMM launch per shape: a CUDA graph of
-    `launches` back-to-back calls over the rotating weight copies, timed with
-    events on the launching stream, median over `reps` replays."""
+    """Average duration (s) of each GEMM launch of a step (one per shape, or
+    one grouped launch): a CUDA graph of `launches` back-to-back calls over the
+    rotating weight copies, timed with events on the launching stream, median
+    over `reps` replays."""
     out = []
-    for si in range(len(wl.shapes)):
-        def chain(si=si):
+    for unit in wl.gemm_units():
+        def chain(fn=unit[3]):
             for i in range(launches):
-                wl.gemm(si, i % wl.copies, stream)
+                fn(i % wl.copies, stream)
         g = capture(chain, stream)
         ts = []
         for _ in range(reps):
@@ -432,15 +464,16 @@ def main() -> None:
     # FP8 ridge point ~560 flop/B (measured tensor / HBM peaks) ~ M = 280 tokens
     bound = "tensor" if M > 280 else "hbm"
     weight_only = args.workload in WEIGHT_ONLY
+    grouped = args.workload in GROUPED
     if weight_only and M > 16:
         ap.error("the weight-only workload is a decode path (M <= 16)")
-    kernel = gemm_kernel_name(M)
+    kernel = "gemm_skinny_grouped_kernel" if grouped else gemm_kernel_name(M)
     if args.workload in WORKLOAD_SHAPES:
         shapes, seeds = WORKLOAD_SHAPES[args.workload]
         weights = Weights(device, shapes=shapes, seed_index=seeds)
     else:
         weights = Weights(device)
-    wl = Workload(M, weights, device, weight_only=weight_only)
+    wl = Workload(M, weights, device, weight_only=weight_only, grouped=grouped)
     graphs = [capture(lambda c=c: wl.enqueue_step(c, stream), stream) for c in range(wl.copies)]
     launches_per_step = wl.launches_per_step()
 
@@ -496,9 +529,11 @@ def main() -> None:
     h2d = sum(x.numel() * 2 for x in wl.x_host)
     d2h = sum(o.numel() * 2 for o in wl.out_host)
 
-    gemm_bytes = [wl.gemm_bytes_of(N, K) for N, K in wl.shapes]
-    gemm_flops = [2.0 * M * N * K for N, K in wl.shapes]
-    traffic = recorded_traffic(kernel, f"{args.workload}_m{M}_mean_of_5")
+    units = wl.gemm_units()
+    gemm_bytes = [u[1] for u in units]
+    gemm_flops = [u[2] for u in units]
+    labels = [u[0] for u in units]
+    traffic = recorded_traffic(kernel, f"{args.workload}_m{M}_" + ("per_launch" if grouped else "mean_of_5"))
     if bound == "tensor":
         achieved = sum(gemm_flops) / sum(gemm_ts) / 1e12
         # a millisecond-long GEMM inside a long step runs under the power cap:
@@ -507,17 +542,17 @@ def main() -> None:
         peak_kind = (f"{peaks_kind} bf16 dense (cuBLAS, sustained under the power cap) x {FP8_OVER_BF16:g}, "
                      "the nominal FP8/bf16 ratio")
         roof_unit, per_launch = "TFLOP/s", {"flops_per_launch": sum(gemm_flops) / len(gemm_flops)}
-        per_shape = [{"N": N, "K": K, "us_per_call": round(t * 1e6, 3), "tflops": round(f / t / 1e12, 1),
+        per_shape = [{**_label(lb), "us_per_call": round(t * 1e6, 3), "tflops": round(f / t / 1e12, 1),
                       "frac": round(f / t / 1e12 / peak, 4)}
-                     for (N, K), t, f in zip(wl.shapes, gemm_ts, gemm_flops)]
+                     for lb, t, f in zip(labels, gemm_ts, gemm_flops)]
     else:
         achieved = sum(gemm_bytes) / sum(gemm_ts) / 1e9
         peak = float(peaks["hbm_gbs"])
         peak_kind = f"{peaks_kind} HBM copy bandwidth"
         roof_unit, per_launch = "GB/s", {"bytes_per_launch": sum(gemm_bytes) / len(gemm_bytes)}
-        per_shape = [{"N": N, "K": K, "us_per_call": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1),
+        per_shape = [{**_label(lb), "us_per_call": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1),
                       "frac": round(b / t / 1e9 / peak, 4)}
-                     for (N, K), t, b in zip(wl.shapes, gemm_ts, gemm_bytes)]
+                     for lb, t, b in zip(labels, gemm_ts, gemm_bytes)]
 
     del graphs
     torch.cuda.synchronize()
@@ -544,7 +579,7 @@ def main() -> None:
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 5)},
         "clocks": clk.summary(),
     }
-    if not args.no_sweep and rank == 0 and not weight_only and args.workload not in WORKLOAD_SHAPES:
+    if not args.no_sweep and rank == 0 and not weight_only and not grouped and args.workload not in WORKLOAD_SHAPES:
         del wl
         torch.cuda.empty_cache()
         result["sweep"] = sweep(weights, device, stream, peaks)

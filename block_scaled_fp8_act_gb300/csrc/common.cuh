@@ -43,6 +43,11 @@ __device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
     return v;
 }
 
+// Hint: bring the 128-byte line holding `p` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // 16-byte load of data that many CTAs re-read (kept in L1).
 __device__ __forceinline__ uint4 ld_shared_ro_v4(const void* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));

@@ -68,6 +68,54 @@ int gemm_common(const void* q, const float* sa, const void* w, const float* sw, 
     return launch_status(fp8act::launch_gemm_tc(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
 }
 
+constexpr int kMaxGrouped = 16;
+
+// The single-call checks of one GEMM problem (no launch); OK for an empty one.
+int check_gemm(const fp8act_gemm_problem& p) {
+    if (p.M < 0 || p.N < 0) return FP8ACT_ERR_SHAPE;
+    if (int st = check_k(p.K)) return st;
+    if (p.M == 0 || p.N == 0) return FP8ACT_OK;
+    if (!p.q_e4m3 || !p.sa || !p.w_e4m3 || !p.sw || !p.out) return FP8ACT_ERR_NULL;
+    if (!aligned(p.q_e4m3, 16) || !aligned(p.w_e4m3, 16) || !aligned(p.out, 16) || !aligned(p.sa, 4) ||
+        !aligned(p.sw, 4))
+        return FP8ACT_ERR_ALIGN;
+    return FP8ACT_OK;
+}
+
+int gemm_grouped_common(const fp8act_gemm_problem* problems, int count, bool out_f32, void* stream) {
+    if (count < 0 || count > kMaxGrouped) return FP8ACT_ERR_SHAPE;
+    if (count == 0) return FP8ACT_OK;
+    if (!problems) return FP8ACT_ERR_NULL;
+    bool any = false;
+    for (int i = 0; i < count; ++i) {
+        if (int st = check_gemm(problems[i])) return st;
+        any = any || (problems[i].M > 0 && problems[i].N > 0);
+    }
+    if (!any) return FP8ACT_OK;
+    int st = FP8ACT_OK;
+    const int sms = current_device_sms(&st);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    fp8act::GemmProblem skinny[kMaxGrouped];
+    int n_skinny = 0;
+    for (int i = 0; i < count; ++i) {
+        const fp8act_gemm_problem& p = problems[i];
+        if (p.M == 0 || p.N == 0 || p.M > kSkinnyMaxM) continue;
+        skinny[n_skinny++] = {static_cast<const uint8_t*>(p.q_e4m3), p.sa, static_cast<const uint8_t*>(p.w_e4m3),
+                              p.sw, p.out, p.M, p.N, p.K};
+    }
+    if (int e = launch_status(fp8act::launch_gemm_skinny_grouped(skinny, n_skinny, out_f32, s))) return e;
+    for (int i = 0; i < count; ++i) {
+        const fp8act_gemm_problem& p = problems[i];
+        if (p.M <= kSkinnyMaxM || p.N == 0) continue;
+        if (int e = launch_status(fp8act::launch_gemm_tc(static_cast<const uint8_t*>(p.q_e4m3), p.sa,
+                                                         static_cast<const uint8_t*>(p.w_e4m3), p.sw, p.M, p.N, p.K,
+                                                         p.out, out_f32, sms, s)))
+            return e;
+    }
+    return FP8ACT_OK;
+}
+
 int w8a16_common(const void* x, const void* w, const float* sw, int M, int N, int K, void* out, bool out_f32,
                  void* stream) {
     if (M < 0 || N < 0) return FP8ACT_ERR_SHAPE;
@@ -128,6 +176,36 @@ int fp8_block_gemm_w8a16(const void* x_bf16, const void* w_e4m3, const float* sw
 int fp8_block_gemm_w8a16_f32(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N, int K,
                              float* out_f32, void* stream) {
     return w8a16_common(x_bf16, w_e4m3, sw, M, N, K, out_f32, true, stream);
+}
+
+int fp8_act_quant_grouped(const fp8act_quant_problem* problems, int count, void* stream) {
+    if (count < 0 || count > kMaxGrouped) return FP8ACT_ERR_SHAPE;
+    if (count == 0) return FP8ACT_OK;
+    if (!problems) return FP8ACT_ERR_NULL;
+    fp8act::ActQuantProblem probs[kMaxGrouped];
+    int n = 0;
+    for (int i = 0; i < count; ++i) {
+        const fp8act_quant_problem& p = problems[i];
+        if (p.M < 0) return FP8ACT_ERR_SHAPE;
+        if (int st = check_k(p.K)) return st;
+        if (p.M == 0) continue;
+        if (!p.x_bf16 || !p.q_e4m3 || !p.sa) return FP8ACT_ERR_NULL;
+        if (!aligned(p.x_bf16, 16) || !aligned(p.q_e4m3, 16) || !aligned(p.sa, 4)) return FP8ACT_ERR_ALIGN;
+        probs[n++] = {p.x_bf16, p.q_e4m3, p.sa, p.M, p.K};
+    }
+    if (n == 0) return FP8ACT_OK;
+    int st = FP8ACT_OK;
+    const int sms = current_device_sms(&st);
+    if (st) return st;
+    return launch_status(fp8act::launch_act_quant_grouped(probs, n, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_block_gemm_grouped(const fp8act_gemm_problem* problems, int count, void* stream) {
+    return gemm_grouped_common(problems, count, false, stream);
+}
+
+int fp8_block_gemm_grouped_f32(const fp8act_gemm_problem* problems, int count, void* stream) {
+    return gemm_grouped_common(problems, count, true, stream);
 }
 
 const char* fp8act_strerror(int status) {

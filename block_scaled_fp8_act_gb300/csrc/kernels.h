@@ -11,6 +11,16 @@ namespace fp8act {
 cudaError_t launch_act_quant(const void* x, int64_t M, int64_t K, void* q, float* sa, int num_sms,
                              cudaStream_t stream);
 
+// One activation-quantisation problem: x bf16 [M, K] -> q [M, K], sa [M, K/128].
+struct ActQuantProblem {
+    const void* x;
+    void* q;
+    float* sa;
+    int64_t M, K;
+};
+// Up to 16 of them in one launch (their 128-wide groups concatenated).
+cudaError_t launch_act_quant_grouped(const ActQuantProblem* probs, int count, int num_sms, cudaStream_t stream);
+
 // Weight quantisation, W bf16 [N, K] -> w E4M3 [N, K], sw fp32 [ceil(N/128), K/128].
 cudaError_t launch_weight_quant(const void* W, int64_t N, int64_t K, void* w, float* sw, cudaStream_t stream);
 
@@ -29,6 +39,20 @@ cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const u
 // activation scales (E4M3 weights widened to bf16, bf16 MMAs).
 cudaError_t launch_gemm_w8a16(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
                               bool out_f32, int num_sms, cudaStream_t stream);
+
+// One block-FP8 GEMM problem (device pointers, row-major, as fp8_block_gemm).
+struct GemmProblem {
+    const uint8_t* q;
+    const float* sa;
+    const uint8_t* w;
+    const float* sw;
+    void* out;
+    int M, N, K;
+};
+
+// Up to 16 independent problems with M <= 16 in one launch of the
+// weight-streaming kernel (each CTA finds its problem from its index).
+cudaError_t launch_gemm_skinny_grouped(const GemmProblem* probs, int count, bool out_f32, cudaStream_t stream);
 
 // Tensor-memory (tcgen05) GEMM: 128 x 256 (prefill) or 128 x 128 output
 // tiles, TMA-fed ring, per-K-group promotion of the fp32 block scales in the

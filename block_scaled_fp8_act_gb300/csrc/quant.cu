@@ -21,9 +21,46 @@ namespace {
 // Groups are contiguous in memory because K % 128 == 0, so group g of the
 // flattened [M*K/128] index starts at element 128 g and its scale is sa[g].
 constexpr int kActUnroll = 2;
+constexpr int kMaxActProblems = 16;
 
-__global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict__ x, int64_t groups,
-                                                        uint2* __restrict__ q, float* __restrict__ sa) {
+// Where group g of the flattened index lives: one problem ...
+struct ActSingle {
+    const uint4* x;
+    uint2* q;
+    float* sa;
+    __device__ __forceinline__ void at(int64_t g, const uint4*& xg, uint2*& qg, float*& sg) const {
+        xg = x + g * 16;
+        qg = q + g * 16;
+        sg = sa + g;
+    }
+};
+
+// ... or several, concatenated: problem i owns groups [begin_i, begin_{i+1}).
+struct ActGroupedProblem {
+    const uint4* x;
+    uint2* q;
+    float* sa;
+    int64_t begin;
+};
+struct ActGroupedArgs {
+    ActGroupedProblem p[kMaxActProblems];
+    int count;
+    int64_t groups;
+};
+struct ActGrouped {
+    const ActGroupedArgs* a;
+    __device__ __forceinline__ void at(int64_t g, const uint4*& xg, uint2*& qg, float*& sg) const {
+        int i = 0;
+        while (i + 1 < a->count && g >= a->p[i + 1].begin) ++i;
+        const int64_t l = g - a->p[i].begin;
+        xg = a->p[i].x + l * 16;
+        qg = a->p[i].q + l * 16;
+        sg = a->p[i].sa + l;
+    }
+};
+
+template <class Map>
+__device__ __forceinline__ void act_quant_body(const Map& map, int64_t groups) {
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4;
     const int hl = lane & 15;
@@ -38,10 +75,16 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict_
     ptx::griddep_wait();
     for (int64_t base = warp * per_iter; base < groups; base += nwarp * per_iter) {
         uint4 v[kActUnroll];
+        uint2* qg[kActUnroll];
+        float* sg[kActUnroll];
 #pragma unroll
         for (int u = 0; u < kActUnroll; ++u) {
             const int64_t g = base + 2 * u + half;
-            v[u] = g < groups ? ld_stream_v4(x + g * 16 + hl) : make_uint4(0, 0, 0, 0);
+            const uint4* xg = nullptr;
+            qg[u] = nullptr;
+            sg[u] = nullptr;
+            if (g < groups) map.at(g, xg, qg[u], sg[u]);
+            v[u] = g < groups ? ld_stream_v4(xg + hl) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kActUnroll; ++u) {
@@ -62,11 +105,20 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict_
             for (int i = 0; i < 4; ++i)
                 c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
             if (g < groups) {
-                q[g * 16 + hl] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-                if (hl == 0) sa[g] = s;
+                qg[u][hl] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+                if (hl == 0) *sg[u] = s;
             }
         }
     }
+}
+
+__global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict__ x, int64_t groups,
+                                                        uint2* __restrict__ q, float* __restrict__ sa) {
+    act_quant_body(ActSingle{x, q, sa}, groups);
+}
+
+__global__ void __launch_bounds__(256) act_quant_grouped_kernel(const __grid_constant__ ActGroupedArgs a) {
+    act_quant_body(ActGrouped{&a}, a.groups);
 }
 
 // One CTA of 256 threads per 128x128 weight block. Warp w holds rows
@@ -114,23 +166,51 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __res
 
 }  // namespace
 
-cudaError_t launch_act_quant(const void* x, int64_t M, int64_t K, void* q, float* sa, int num_sms,
-                             cudaStream_t stream) {
-    const int64_t groups = M * (K / kGroup);
+static cudaError_t act_quant_config(int64_t groups, int num_sms, cudaStream_t stream, cudaLaunchConfig_t& cfg,
+                             cudaLaunchAttribute (&attr)[1]) {
     const int threads = 256;
     const int64_t groups_per_block = (threads / 32) * 2 * kActUnroll;
     int64_t blocks = (groups + groups_per_block - 1) / groups_per_block;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    cudaLaunchConfig_t cfg = {};
+    cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
     cfg.blockDim = dim3(threads);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cudaSuccess;
+}
+
+cudaError_t launch_act_quant_grouped(const ActQuantProblem* probs, int count, int num_sms, cudaStream_t stream) {
+    if (count <= 0) return cudaSuccess;
+    if (count > kMaxActProblems) return cudaErrorInvalidValue;
+    ActGroupedArgs a = {};
+    int64_t groups = 0;
+    for (int i = 0; i < count; ++i) {
+        a.p[i].x = static_cast<const uint4*>(probs[i].x);
+        a.p[i].q = static_cast<uint2*>(probs[i].q);
+        a.p[i].sa = probs[i].sa;
+        a.p[i].begin = groups;
+        groups += probs[i].M * (probs[i].K / kGroup);
+    }
+    a.count = count;
+    a.groups = groups;
+    if (groups == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    act_quant_config(groups, num_sms, stream, cfg, attr);
+    return cudaLaunchKernelEx(&cfg, act_quant_grouped_kernel, a);
+}
+
+cudaError_t launch_act_quant(const void* x, int64_t M, int64_t K, void* q, float* sa, int num_sms,
+                             cudaStream_t stream) {
+    const int64_t groups = M * (K / kGroup);
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    act_quant_config(groups, num_sms, stream, cfg, attr);
     return cudaLaunchKernelEx(&cfg, act_quant_kernel, static_cast<const uint4*>(x), groups,
                               static_cast<uint2*>(q), sa);
 }

@@ -55,11 +55,15 @@ def load(build: bool = False) -> ctypes.CDLL:
     L.fp8_block_gemm_f32.argtypes = [p, p, p, p, i, i, i, p, p]
     L.fp8_block_gemm_w8a16.argtypes = [p, p, p, i, i, i, p, p]
     L.fp8_block_gemm_w8a16_f32.argtypes = [p, p, p, i, i, i, p, p]
+    L.fp8_act_quant_grouped.argtypes = [p, i, p]
+    L.fp8_block_gemm_grouped.argtypes = [p, i, p]
+    L.fp8_block_gemm_grouped_f32.argtypes = [p, i, p]
     L.fp8act_strerror.argtypes = [i]
     L.fp8act_strerror.restype = ctypes.c_char_p
     L.fp8act_check_status.argtypes = [p]
     for fn in (L.fp8_act_quant, L.fp8_weight_quant, L.fp8_block_gemm, L.fp8_block_gemm_f32,
                L.fp8_block_gemm_w8a16, L.fp8_block_gemm_w8a16_f32,
+               L.fp8_act_quant_grouped, L.fp8_block_gemm_grouped, L.fp8_block_gemm_grouped_f32,
                L.fp8act_check_status, L.fp8act_version):
         fn.restype = ctypes.c_int
     _lib = L
@@ -175,6 +179,81 @@ def fp8_block_gemm_w8a16(x, w, sw, out=None, stream=None) -> torch.Tensor:
 def fp8_block_gemm_w8a16_f32(x, w, sw, out=None, stream=None) -> torch.Tensor:
     """fp32 [M, N] output of the weight-only kernels (no bf16 cast)."""
     return _gemm_w8a16("fp8_block_gemm_w8a16_f32", torch.float32, x, w, sw, out, stream)
+
+
+class QuantProblem(ctypes.Structure):
+    """fp8act_quant_problem of include/fp8act.h."""
+    _fields_ = [("x_bf16", ctypes.c_void_p), ("q_e4m3", ctypes.c_void_p), ("sa", ctypes.c_void_p),
+                ("M", ctypes.c_int), ("K", ctypes.c_int)]
+
+
+class GemmProblem(ctypes.Structure):
+    """fp8act_gemm_problem of include/fp8act.h."""
+    _fields_ = [("q_e4m3", ctypes.c_void_p), ("sa", ctypes.c_void_p), ("w_e4m3", ctypes.c_void_p),
+                ("sw", ctypes.c_void_p), ("out", ctypes.c_void_p), ("M", ctypes.c_int), ("N", ctypes.c_int),
+                ("K", ctypes.c_int)]
+
+
+MAX_GROUPED = 16
+
+
+def fp8_act_quant_grouped(xs, outs=None, stream=None):
+    """Quantise several bf16 activations [M_i, K_i] in one launch.
+
+    Returns [(q_i, sa_i)]; `outs` may supply them."""
+    if len(xs) > MAX_GROUPED:
+        raise ValueError(f"at most {MAX_GROUPED} problems per grouped call")
+    res = []
+    arr = (QuantProblem * max(1, len(xs)))()
+    for i, x in enumerate(xs):
+        _cuda2d(x, (torch.bfloat16,), "x")
+        M, K = x.shape
+        if outs is None:
+            q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+            sa = torch.empty((M, K // G), dtype=torch.float32, device=x.device)
+        else:
+            q, sa = outs[i]
+        _cuda2d(q, _CODES, "q")
+        _cuda2d(sa, (torch.float32,), "sa")
+        if q.shape != (M, K) or sa.shape != (M, K // G):
+            raise ValueError("q / sa have the wrong shape")
+        arr[i] = QuantProblem(x.data_ptr(), q.data_ptr(), sa.data_ptr(), M, K)
+        res.append((q, sa))
+    _check("fp8_act_quant_grouped", load().fp8_act_quant_grouped(ctypes.byref(arr), len(xs), _stream(stream)))
+    return res
+
+
+def _gemm_grouped(fn_name: str, out_dtype, problems, outs, stream):
+    if len(problems) > MAX_GROUPED:
+        raise ValueError(f"at most {MAX_GROUPED} problems per grouped call")
+    res = []
+    arr = (GemmProblem * max(1, len(problems)))()
+    for i, (q, sa, w, sw) in enumerate(problems):
+        for t, n, d in ((q, "q", _CODES), (sa, "sa", (torch.float32,)), (w, "w", _CODES),
+                        (sw, "sw", (torch.float32,))):
+            _cuda2d(t, d, n)
+        M, K = q.shape
+        N = w.shape[0]
+        if w.shape[1] != K or sa.shape != (M, K // G) or sw.shape != ((N + G - 1) // G, K // G):
+            raise ValueError("inconsistent q / sa / w / sw shapes")
+        out = torch.empty((M, N), dtype=out_dtype, device=q.device) if outs is None else outs[i]
+        _cuda2d(out, (out_dtype,), "out")
+        if out.shape != (M, N):
+            raise ValueError("out has the wrong shape")
+        arr[i] = GemmProblem(q.data_ptr(), sa.data_ptr(), w.data_ptr(), sw.data_ptr(), out.data_ptr(), M, N, K)
+        res.append(out)
+    _check(fn_name, getattr(load(), fn_name)(ctypes.byref(arr), len(problems), _stream(stream)))
+    return res
+
+
+def fp8_block_gemm_grouped(problems, outs=None, stream=None) -> list:
+    """Several block GEMMs [(q, sa, w, sw), ...] in one launch; returns the bf16 outputs."""
+    return _gemm_grouped("fp8_block_gemm_grouped", torch.bfloat16, problems, outs, stream)
+
+
+def fp8_block_gemm_grouped_f32(problems, outs=None, stream=None) -> list:
+    """fp32 outputs of the grouped kernels (no bf16 cast)."""
+    return _gemm_grouped("fp8_block_gemm_grouped_f32", torch.float32, problems, outs, stream)
 
 
 def check_status(stream=None) -> int:

@@ -122,6 +122,52 @@ FP8ACT_API int fp8_block_gemm_w8a16(const void* x_bf16, const void* w_e4m3, cons
 FP8ACT_API int fp8_block_gemm_w8a16_f32(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N,
                                         int K, float* out_f32, void* stream);
 
+/*
+ * Grouped calls: several independent problems in one kernel launch.
+ * The zskr.cn decode-optimisation article on Qwen3-27B, section 3.3
+ * ("第三板斧"), merges the Q, K and V matmuls into one operator to save
+ * launches, and the single-RTX-PRO-6000 Qwen3.8-27B post counts about 176
+ * launches per decode step. A single launch also streams the problems'
+ * weights back to back, with no ramp-up or tail between them.
+ * (Projections that share their input can also be concatenated along N
+ * into one ordinary call: weight rows of each part must start on a
+ * 128-row block boundary so that the scale blocks do not straddle parts.)
+ *
+ * `problems` is a HOST array of `count` entries (0 <= count <= 16), read
+ * during the call only. Each entry follows the rules of the single call
+ * (pointers, alignment, K % 128 == 0); entries with M == 0 or N == 0 are
+ * skipped. Problems must not write overlapping outputs. Errors: the first
+ * invalid entry's status, before anything is launched; FP8ACT_ERR_SHAPE for
+ * count < 0 or count > 16; FP8ACT_ERR_NULL for problems == NULL with
+ * count > 0.
+ */
+typedef struct {
+    const void* x_bf16; /* [M, K] bf16 in           */
+    void* q_e4m3;       /* [M, K] E4M3 codes out    */
+    float* sa;          /* [M, K/128] fp32 scales out */
+    int M, K;
+} fp8act_quant_problem;
+
+typedef struct {
+    const void* q_e4m3; /* [M, K] activation codes               */
+    const float* sa;    /* [M, K/128] activation scales          */
+    const void* w_e4m3; /* [N, K] weight codes                   */
+    const float* sw;    /* [ceil(N/128), K/128] weight scales    */
+    void* out;          /* [M, N] bf16 (fp32 for the _f32 call)  */
+    int M, N, K;
+} fp8act_gemm_problem;
+
+/* fp8_act_quant over every problem, one launch. Bit-exact with it. */
+FP8ACT_API int fp8_act_quant_grouped(const fp8act_quant_problem* problems, int count, void* stream);
+
+/*
+ * fp8_block_gemm over every problem. The problems with M <= 16 share one
+ * launch of the weight-streaming kernel (largest weights first); any with
+ * M > 16 follow on the same stream, one tile-kernel launch each.
+ */
+FP8ACT_API int fp8_block_gemm_grouped(const fp8act_gemm_problem* problems, int count, void* stream);
+FP8ACT_API int fp8_block_gemm_grouped_f32(const fp8act_gemm_problem* problems, int count, void* stream);
+
 /* A static English description of a status code (never NULL). */
 FP8ACT_API const char* fp8act_strerror(int status);
 

@@ -22,6 +22,7 @@ def test_library_exports_every_header_symbol(lib):
     names = fp8act.header_symbols()
     assert {"fp8_act_quant", "fp8_weight_quant", "fp8_block_gemm", "fp8_block_gemm_f32",
             "fp8_block_gemm_w8a16", "fp8_block_gemm_w8a16_f32",
+            "fp8_act_quant_grouped", "fp8_block_gemm_grouped", "fp8_block_gemm_grouped_f32",
             "fp8act_strerror", "fp8act_check_status", "fp8act_version"} <= set(names)
     raw = ctypes.CDLL(fp8act.lib_path())
     for n in names:
@@ -91,3 +92,49 @@ def test_w8a16_argument_checks(lib, name):
     assert f(A16 + 8, A16, A16, 1, 128, 128, A16, None) == ALIGN
     assert f(A16, A16, A16 + 2, 1, 128, 128, A16, None) == ALIGN
     assert f(A16, A16, A16, 1, 128, 128, A16 + 4, None) == ALIGN
+
+
+def test_grouped_structs_match_the_header():
+    import re
+    import os
+    text = open(os.path.join(fp8build.INCLUDE, "fp8act.h"), encoding="utf-8").read()
+    for cname, py in (("fp8act_quant_problem", fp8act.QuantProblem), ("fp8act_gemm_problem", fp8act.GemmProblem)):
+        body = re.search(r"typedef struct \{([^{}]*)\}\s*" + cname + ";", text).group(1)
+        names = re.findall(r"(\w+)(?:,|;)", re.sub(r"/\*.*?\*/", "", body, flags=re.S))
+        assert names == [f[0] for f in py._fields_], (cname, names)
+    assert ctypes.sizeof(fp8act.QuantProblem) == 32
+    assert ctypes.sizeof(fp8act.GemmProblem) == 56
+
+
+@pytest.mark.parametrize("name", ["fp8_block_gemm_grouped", "fp8_block_gemm_grouped_f32"])
+def test_gemm_grouped_argument_checks(lib, name):
+    f = getattr(lib, name)
+    P = fp8act.GemmProblem
+    assert f(None, 0, None) == OK
+    assert f(None, 2, None) == NULL
+    arr = (P * 17)()
+    assert f(ctypes.byref(arr), 17, None) == SHAPE
+    assert f(ctypes.byref(arr), -1, None) == SHAPE
+    good = P(A16, A16, A16, A16, A16, 1, 128, 128)
+    arr = (P * 3)(good, P(A16, A16, A16, A16, A16, 1, 128, 64), good)
+    assert f(ctypes.byref(arr), 3, None) == SHAPE       # second entry: K % 128
+    arr = (P * 2)(good, P(A16, A16, None, A16, A16, 1, 128, 128))
+    assert f(ctypes.byref(arr), 2, None) == NULL
+    arr = (P * 2)(good, P(A16, A16, A16 + 8, A16, A16, 1, 128, 128))
+    assert f(ctypes.byref(arr), 2, None) == ALIGN
+    arr = (P * 2)(P(None, None, None, None, None, 0, 128, 128), P(None, None, None, None, None, 3, 0, 256))
+    assert f(ctypes.byref(arr), 2, None) == OK           # only empty problems: nothing to launch
+
+
+def test_act_quant_grouped_argument_checks(lib):
+    f = lib.fp8_act_quant_grouped
+    P = fp8act.QuantProblem
+    assert f(None, 0, None) == OK
+    assert f(None, 1, None) == NULL
+    good = P(A16, A16, A16, 1, 128)
+    arr = (P * 2)(good, P(A16, A16, A16, 1, 100))
+    assert f(ctypes.byref(arr), 2, None) == SHAPE
+    arr = (P * 2)(good, P(A16, A16 + 4, A16, 1, 128))
+    assert f(ctypes.byref(arr), 2, None) == ALIGN
+    arr = (P * 1)(P(None, None, None, 0, 128))
+    assert f(ctypes.byref(arr), 1, None) == OK

@@ -244,3 +244,43 @@ def test_vocab_head_gemv(fp8act, vocab_problem, M):
 
 def test_vocab_head_w8a16(fp8act, vocab_problem):
     _w8a16_compare(fp8act, vocab_problem, 1, seed=711)
+
+
+# ------------------------------------------------------------ grouped calls
+def test_act_quant_grouped_bit_exact(fp8act):
+    """One launch over the five K's and ragged M's, bit-exact per problem."""
+    specs = [(1, 5120), (8, 3072), (3, 8704), (16, 5120), (102, 5120), (0, 256), (5, 128)]
+    xs = [inputs.activations_bf16(M, K, seed=40 + i) for i, (M, K) in enumerate(specs)]
+    res = fp8act.fp8_act_quant_grouped([x.cuda() for x in xs])
+    torch.cuda.synchronize()
+    for x, (q, sa) in zip(xs, res):
+        q_ref, sa_ref = oracle.act_quant(inputs.bf16_bits(x))
+        assert np.array_equal(q.cpu().numpy(), q_ref)
+        assert np.array_equal(sa.cpu().numpy(), sa_ref)
+
+
+def _grouped_compare(fp8act, probs, ms, seed):
+    from parity_util import compare_gemm
+    acts = [p.activations(M, seed + i) for i, (p, M) in enumerate(zip(probs, ms))]
+    args = [(q, sa, p.w, p.sw) for (q, sa, _, _), p in zip(acts, probs)]
+    outs = fp8act.fp8_block_gemm_grouped(args)
+    outs32 = fp8act.fp8_block_gemm_grouped_f32(args)
+    torch.cuda.synchronize()
+    for (q, sa, q_ref, sa_ref), p, o, o32 in zip(acts, probs, outs, outs32):
+        assert np.array_equal(q.cpu().numpy(), q_ref) and np.array_equal(sa.cpu().numpy(), sa_ref)
+        y, aabs, ref = oracle.block_gemm(q_ref, sa_ref, p.w_ref, p.sw_ref)
+        compare_gemm(o, o32, y, aabs, ref, p.K)
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_gemm_grouped_five_shapes(fp8act, M):
+    _grouped_compare(fp8act, [problem(si) for si in range(len(SHAPES))], [M] * len(SHAPES), seed=800 + M)
+
+
+def test_gemm_grouped_ragged_mix(fp8act):
+    """Different M per problem (1..16, and 40 on the tile kernel), N that is
+    not a multiple of 16 or 128, K from 1 to 9 groups."""
+    from parity_util import Problem
+    dims = [(17, 128, 1), (200, 256, 5), (1000, 384, 12), (257, 768, 16), (130, 1152, 3), (300, 512, 40)]
+    probs = [Problem(N, K, seed=900 + i) for i, (N, K, _) in enumerate(dims)]
+    _grouped_compare(fp8act, probs, [m for _, _, m in dims], seed=910)
