@@ -23,6 +23,8 @@ Printed JSON line (rank 0):
 4096; `--workload decode-w8a16` times the weight-only variant at M = 1 (bf16
 activations straight into the GEMM, no quantisation launch); `--workload
 lmhead` times one vocabulary-sized head (N = 151936, K = 5120) at M = 1.
+`--workload decode-fused` runs one fused fp8_linear launch per shape (the
+activation quantisation inside the GEMM kernel).
 `--workload decode-grouped` runs the five projections as independent problems
 of one grouped act-quant launch and one grouped GEMM launch.
 `--impl reference` times the CPU oracle instead (the reference arm).
@@ -63,6 +65,8 @@ WORKLOADS = {
     "decode-w8a16": (1, "weight-only decode M={M} over the five dense-27B projection shapes "
                         "(bf16 activations x block-FP8 weights, one GEMM per shape, no act quant)", "hbm"),
     "lmhead": (1, "vocabulary-sized head M={M}: N=151936, K=5120 (act quant + block-FP8 GEMM)", "hbm"),
+    "decode-fused": (1, "fused decode M={M} over the five dense-27B projection shapes "
+                        "(one fp8_linear launch per shape: act quant inside the block-FP8 GEMM)", "hbm"),
     "decode-grouped": (1, "grouped decode M={M}: the five dense-27B projection shapes as independent problems, "
                           "one grouped act-quant launch + one grouped block-FP8 GEMM launch", "hbm"),
 }
@@ -70,6 +74,7 @@ GROUPED = {"decode-grouped"}
 # Workloads on other shapes than the five projections: (shapes, weight seed indices).
 WORKLOAD_SHAPES = {"lmhead": ((inputs.VOCAB_SHAPE,), (inputs.VOCAB_SEED_INDEX,))}
 WEIGHT_ONLY = {"decode-w8a16"}
+FUSED = {"decode-fused"}
 
 
 def gemm_kernel_name(M: int) -> str:
@@ -217,10 +222,12 @@ class Workload:
     host copies for the end-to-end leg), sharing one Weights set."""
 
     def __init__(self, M: int, weights: Weights, device: torch.device, weight_only: bool = False,
-                 grouped: bool = False):
+                 grouped: bool = False, fused: bool = False):
         self.M = M
         self.weight_only = weight_only
         self.grouped = grouped
+        self.fused = fused
+        self.bf16_in = weight_only or fused  # the GEMM reads the bf16 activations itself
         self.shapes = weights.shapes
         self.copies = weights.copies
         self.w, self.sw = weights.w, weights.sw
@@ -237,16 +244,16 @@ class Workload:
         torch.cuda.synchronize()
 
     def gemm_bytes_of(self, N: int, K: int) -> int:
-        return (algorithmic_w8a16_bytes if self.weight_only else algorithmic_gemm_bytes)(self.M, N, K)
+        return (algorithmic_w8a16_bytes if self.bf16_in else algorithmic_gemm_bytes)(self.M, N, K)
 
     def step_bytes(self) -> int:
-        return sum(self.gemm_bytes_of(N, K) + (0 if self.weight_only else algorithmic_quant_bytes(self.M, K))
+        return sum(self.gemm_bytes_of(N, K) + (0 if self.bf16_in else algorithmic_quant_bytes(self.M, K))
                    for N, K in self.shapes)
 
     def launches_per_step(self) -> int:
         if self.grouped:
             return 2
-        return (1 if self.weight_only else 2) * len(self.shapes)
+        return (1 if self.bf16_in else 2) * len(self.shapes)
 
     def gemm_units(self) -> list:
         """The GEMM launches of one step: (label, algorithmic bytes, flops, enqueue(copy, stream))."""
@@ -266,6 +273,8 @@ class Workload:
         if self.weight_only:
             fp8act.fp8_block_gemm_w8a16(self.x[si], self.w[si][copy], self.sw[si][copy], self.out[si],
                                         stream=stream)
+        elif self.fused:
+            fp8act.fp8_linear(self.x[si], self.w[si][copy], self.sw[si][copy], self.out[si], stream=stream)
         else:
             fp8act.fp8_block_gemm(self.q[si], self.sa[si], self.w[si][copy], self.sw[si][copy],
                                   self.out[si], stream=stream)
@@ -277,7 +286,7 @@ class Workload:
             self.gemm_grouped(copy, stream)
             return
         for si in range(len(self.shapes)):
-            if not self.weight_only:
+            if not self.bf16_in:
                 fp8act.fp8_act_quant(self.x[si], self.q[si], self.sa[si], stream=stream)
             self.gemm(si, copy, stream)
 
@@ -465,15 +474,16 @@ def main() -> None:
     bound = "tensor" if M > 280 else "hbm"
     weight_only = args.workload in WEIGHT_ONLY
     grouped = args.workload in GROUPED
-    if weight_only and M > 16:
-        ap.error("the weight-only workload is a decode path (M <= 16)")
+    fused = args.workload in FUSED
+    if (weight_only or fused) and M > 16:
+        ap.error("the weight-only and fused workloads are decode paths (M <= 16)")
     kernel = "gemm_skinny_grouped_kernel" if grouped else gemm_kernel_name(M)
     if args.workload in WORKLOAD_SHAPES:
         shapes, seeds = WORKLOAD_SHAPES[args.workload]
         weights = Weights(device, shapes=shapes, seed_index=seeds)
     else:
         weights = Weights(device)
-    wl = Workload(M, weights, device, weight_only=weight_only, grouped=grouped)
+    wl = Workload(M, weights, device, weight_only=weight_only, grouped=grouped, fused=fused)
     graphs = [capture(lambda c=c: wl.enqueue_step(c, stream), stream) for c in range(wl.copies)]
     launches_per_step = wl.launches_per_step()
 
@@ -579,7 +589,7 @@ def main() -> None:
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 5)},
         "clocks": clk.summary(),
     }
-    if not args.no_sweep and rank == 0 and not weight_only and not grouped and args.workload not in WORKLOAD_SHAPES:
+    if not args.no_sweep and rank == 0 and args.workload == "decode":
         del wl
         torch.cuda.empty_cache()
         result["sweep"] = sweep(weights, device, stream, peaks)

@@ -116,6 +116,21 @@ int gemm_grouped_common(const fp8act_gemm_problem* problems, int count, bool out
     return FP8ACT_OK;
 }
 
+int linear_common(const void* x, const void* w, const float* sw, int M, int N, int K, void* out, bool out_f32,
+                  void* stream) {
+    if (M < 0 || N < 0) return FP8ACT_ERR_SHAPE;
+    if (int st = check_k(K)) return st;
+    if (M == 0 || N == 0) return FP8ACT_OK;
+    if (!fp8act::fused_fits(M, K)) return FP8ACT_ERR_SHAPE;
+    if (!x || !w || !sw || !out) return FP8ACT_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(out, 16) || !aligned(sw, 4)) return FP8ACT_ERR_ALIGN;
+    int st = FP8ACT_OK;
+    const int sms = current_device_sms(&st);
+    if (st) return st;
+    return launch_status(fp8act::launch_linear_fused(x, static_cast<const uint8_t*>(w), sw, M, N, K, out, out_f32,
+                                                     sms, static_cast<cudaStream_t>(stream)));
+}
+
 int w8a16_common(const void* x, const void* w, const float* sw, int M, int N, int K, void* out, bool out_f32,
                  void* stream) {
     if (M < 0 || N < 0) return FP8ACT_ERR_SHAPE;
@@ -176,6 +191,16 @@ int fp8_block_gemm_w8a16(const void* x_bf16, const void* w_e4m3, const float* sw
 int fp8_block_gemm_w8a16_f32(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N, int K,
                              float* out_f32, void* stream) {
     return w8a16_common(x_bf16, w_e4m3, sw, M, N, K, out_f32, true, stream);
+}
+
+int fp8_linear(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N, int K, void* out_bf16,
+               void* stream) {
+    return linear_common(x_bf16, w_e4m3, sw, M, N, K, out_bf16, false, stream);
+}
+
+int fp8_linear_f32(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N, int K, float* out_f32,
+                   void* stream) {
+    return linear_common(x_bf16, w_e4m3, sw, M, N, K, out_f32, true, stream);
 }
 
 int fp8_act_quant_grouped(const fp8act_quant_problem* problems, int count, void* stream) {

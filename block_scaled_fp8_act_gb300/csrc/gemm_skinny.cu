@@ -34,7 +34,7 @@
 //  - The warps' partial sums meet in shared memory and one pass writes the
 //    16 x M outputs (bf16, or fp32 for the error-analysis entry point).
 //
-// Weight-only mode (kA16): the activations stay bf16 (no quantisation
+// Weight-only mode (kModeA16): the activations stay bf16 (no quantisation
 // launch, the job of the weight-only FP8 back-end that the same post uses at
 // one request, section "单并发优化"). Each lane widens its 32 weight codes of
 // a block to bf16 (E4M3 -> f16 -> f32 -> bf16, exact at every step) and runs
@@ -42,6 +42,16 @@
 // takes codes 4i..4i+3 of the lane's 32 and the lane's activations at the
 // same positions (64 bytes of bf16 per lane and block). Only the weight
 // scale multiplies the block's dot.
+//
+// Fused mode (kModeFQ): bf16 activations in, the layer's full W8A8 result
+// out, in one launch (the quantisation launch per linear layer is what the
+// same post's single-request section credits the weight-only back-end with
+// saving; here the quantisation stays and moves into the GEMM). After the
+// programmatic-launch wait each CTA quantises its <= 8 tokens into shared
+// memory with the activation kernel's own group code (so the codes and
+// scales are the same bits), then runs the W8A8 loop on them. Every CTA
+// repeats the quantisation of the same tokens, so the mode suits small M.
+#include "act_group.cuh"
 #include <atomic>
 
 #include <cuda_fp16.h>
@@ -54,6 +64,13 @@ namespace fp8act {
 namespace {
 
 constexpr int kMaxWarps = 16;
+// Kernel modes: W8A8 (E4M3 activation codes and scales in), weight-only
+// (bf16 activations, widened weights) and fused (bf16 activations quantised
+// by the CTA into shared memory, then the W8A8 loop).
+constexpr int kModeW8A8 = 0;
+constexpr int kModeA16 = 1;
+constexpr int kModeFQ = 2;
+constexpr size_t kFusedMaxSmem = 200 * 1024;  // the fused mode's shared-memory ceiling per CTA
 // L2 prefetch distance, in warp steps: each warp keeps the weight lines of
 // the next steps on their way into L2 (prefetches hold no registers). One
 // step measured best: 10% off the five decode shapes at M = 1 against no
@@ -104,12 +121,16 @@ __device__ __forceinline__ void widen_row(const uint4& lo, const uint4& hi, uint
 // One CTA's work: output rows n0..n0+15 for tokens m0..m0 + 8 kTG - 1.
 // kUnroll = K blocks whose weight loads a warp has in flight at once;
 // kTG = groups of 8 tokens a CTA handles (they share the weight fragments);
-// kA16 = bf16 activations in `q` (weight-only mode; `sa` unused).
-template <bool kF32Out, int kUnroll, int kTG, bool kA16>
+// kMode: kModeW8A8 (codes in `q`, scales in `sa`), kModeA16 (bf16
+// activations in `q`, `sa` unused) or kModeFQ (bf16 activations in `q`,
+// quantised into the dynamic shared memory `fq_smem`: min(8, M) rows of K
+// codes, then their K / 128 scales; `sa` unused; kTG must be 1).
+template <bool kF32Out, int kUnroll, int kTG, int kMode>
 __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const float* __restrict__ sa,
                                             const uint8_t* __restrict__ w, const float* __restrict__ sw, int M,
                                             int N, int K, void* __restrict__ out, int n0, int m0,
-                                            float (*red)[16][8 * kTG]) {
+                                            float (*red)[16][8 * kTG], uint8_t* fq_smem = nullptr) {
+    static_assert(kMode != kModeFQ || kTG == 1, "the fused mode quantises one group of 8 tokens per CTA");
     const int KB = K / kGroup;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -140,7 +161,7 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
     const uint8_t* w_pf = w + static_cast<int64_t>(n0 + lane) * K;
     if (pf_lane) {
 #pragma unroll
-        for (int s = 1; s <= kL2Ahead; ++s)
+        for (int s = kMode == kModeFQ ? 0 : 1; s <= kL2Ahead; ++s)
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int kb = warp + s * stride + u * nwarps;
@@ -148,6 +169,37 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
             }
     }
     bool waited = false;
+    const int fq_rows = M - m0 < 8 ? M - m0 : 8;
+    const uint8_t* q_s = fq_smem;
+    const float* sa_s = reinterpret_cast<const float*>(fq_smem + static_cast<int64_t>(fq_rows) * K);
+    if constexpr (kMode == kModeFQ) {
+        // Quantise this CTA's tokens m0 .. m0 + fq_rows - 1 into shared memory:
+        // half-warp h of warp w takes groups 2 w + h, 2 w + h + 2 nwarps, ...
+        // (row-major over (token, K group)); the whole warp runs every pass
+        // because the group code shuffles across the warp.
+        ptx::griddep_wait();
+        waited = true;
+        uint8_t* q_w = fq_smem;
+        float* sa_w = reinterpret_cast<float*>(fq_smem + static_cast<int64_t>(fq_rows) * K);
+        const int half = lane >> 4;
+        const int hl = lane & 15;
+        const int groups = fq_rows * KB;
+        for (int base = 2 * warp; base < groups; base += 2 * nwarps) {
+            const int gi = base + half;
+            const bool ok = gi < groups;
+            const int r = ok ? gi / KB : 0;
+            const int kb = ok ? gi % KB : 0;
+            const uint4 v = ok ? ld_stream_v4(q + (static_cast<int64_t>(m0 + r) * K + kb * kGroup + 8 * hl) * 2)
+                               : zero;
+            uint2 codes;
+            const float sg = quant_group_halfwarp(v, codes);
+            if (ok) {
+                *reinterpret_cast<uint2*>(q_w + static_cast<int64_t>(r) * K + kb * kGroup + 8 * hl) = codes;
+                if (hl == 0) sa_w[r * KB + kb] = sg;
+            }
+        }
+        __syncthreads();
+    }
     for (int kb0 = warp; kb0 < KB; kb0 += stride) {
         if (pf_lane) {
 #pragma unroll
@@ -171,7 +223,7 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
             ptx::griddep_wait();
             waited = true;
         }
-        if constexpr (kA16) {
+        if constexpr (kMode == kModeA16) {
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int kb = kb0 + u * nwarps;
@@ -211,7 +263,8 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
             for (int j = 0; j < kTG; ++j) {
                 const int m = m0 + 8 * j + g;  // this lane's token for the B fragment
                 const bool ok_x = m < M;
-                const uint8_t* x_r = q + static_cast<int64_t>(m) * K + 16 * t;
+                const uint8_t* x_r = kMode == kModeFQ ? q_s + static_cast<int64_t>(g) * K + 16 * t
+                                                      : q + static_cast<int64_t>(m) * K + 16 * t;
                 const int c0 = m0 + 8 * j + 2 * t;  // token columns of this lane's accumulators
                 uint4 xlo[kUnroll], xhi[kUnroll];
 #pragma unroll
@@ -219,8 +272,13 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                     const int kb = kb0 + u * nwarps;
                     const bool ok_k = kb < KB;
                     const int64_t off = static_cast<int64_t>(kb) * kGroup;
-                    xlo[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off) : zero;
-                    xhi[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off + 64) : zero;
+                    if constexpr (kMode == kModeFQ) {
+                        xlo[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + off) : zero;
+                        xhi[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + off + 64) : zero;
+                    } else {
+                        xlo[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off) : zero;
+                        xhi[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off + 64) : zero;
+                    }
                 }
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
@@ -232,8 +290,16 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                         mma_e4m3_16x8x32(d, r0hi[u].x, r1hi[u].x, r0hi[u].y, r1hi[u].y, xhi[u].x, xhi[u].y);
                         mma_e4m3_16x8x32(d, r0hi[u].z, r1hi[u].z, r0hi[u].w, r1hi[u].w, xhi[u].z, xhi[u].w);
                         const float s_w = __ldg(sw_r + kb);
-                        const float s0 = c0 < M ? __ldg(sa + static_cast<int64_t>(c0) * KB + kb) * s_w : 0.f;
-                        const float s1 = c0 + 1 < M ? __ldg(sa + static_cast<int64_t>(c0 + 1) * KB + kb) * s_w : 0.f;
+                        float sa0 = 0.f, sa1 = 0.f;
+                        if constexpr (kMode == kModeFQ) {
+                            if (c0 < M) sa0 = sa_s[(c0 - m0) * KB + kb];
+                            if (c0 + 1 < M) sa1 = sa_s[(c0 + 1 - m0) * KB + kb];
+                        } else {
+                            if (c0 < M) sa0 = __ldg(sa + static_cast<int64_t>(c0) * KB + kb);
+                            if (c0 + 1 < M) sa1 = __ldg(sa + static_cast<int64_t>(c0 + 1) * KB + kb);
+                        }
+                        const float s0 = sa0 * s_w;
+                        const float s1 = sa1 * s_w;
                         acc[j][0] = fmaf(d[0], s0, acc[j][0]);
                         acc[j][1] = fmaf(d[1], s1, acc[j][1]);
                         acc[j][2] = fmaf(d[2], s0, acc[j][2]);
@@ -270,13 +336,14 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
     }
 }
 
-template <bool kF32Out, int kUnroll, int kTG, bool kA16 = false>
+template <bool kF32Out, int kUnroll, int kTG, int kMode = kModeW8A8>
 __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
     const uint8_t* __restrict__ q, const float* __restrict__ sa, const uint8_t* __restrict__ w,
     const float* __restrict__ sw, int M, int N, int K, void* __restrict__ out) {
     __shared__ float red[kMaxWarps][16][8 * kTG];
-    skinny_tile<kF32Out, kUnroll, kTG, kA16>(q, sa, w, sw, M, N, K, out, blockIdx.x * 16, blockIdx.y * 8 * kTG,
-                                             red);
+    extern __shared__ __align__(16) uint8_t fq_smem[];
+    skinny_tile<kF32Out, kUnroll, kTG, kMode>(q, sa, w, sw, M, N, K, out, blockIdx.x * 16, blockIdx.y * 8 * kTG,
+                                              red, fq_smem);
 }
 
 // Several independent problems in one grid: CTA b belongs to the problem p
@@ -305,27 +372,34 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_grouped_kernel(con
     while (i + 1 < a.count && b >= a.p[i + 1].begin) ++i;
     const GroupedProblem& p = a.p[i];
     const int local = b - p.begin;
-    skinny_tile<kF32Out, kUnroll, 1, false>(p.q, p.sa, p.w, p.sw, p.M, p.N, p.K, p.out, (local % p.tiles_n) * 16,
+    skinny_tile<kF32Out, kUnroll, 1, kModeW8A8>(p.q, p.sa, p.w, p.sw, p.M, p.N, p.K, p.out, (local % p.tiles_n) * 16,
                                             (local / p.tiles_n) * 8, red);
 }
 
+// Dynamic shared memory of the fused mode: min(8, M) rows of K codes and of
+// K / 128 fp32 scales.
+size_t fused_smem_bytes(int M, int K) {
+    const size_t rows = M < 8 ? M : 8;
+    return rows * (static_cast<size_t>(K) + 4 * static_cast<size_t>(K / kGroup));
+}
+
 // CTAs per SM for a (load depth, token groups, warps) configuration, from the
-// occupancy API, cached per device.
-template <bool kF32Out, int kUnroll, int kTG, bool kA16>
-int ctas_per_sm(int wv) {
+// occupancy API; cached per device when the CTA uses no dynamic shared memory.
+template <bool kF32Out, int kUnroll, int kTG, int kMode>
+int ctas_per_sm(int wv, size_t smem) {
     static std::atomic<int> cache[64][kMaxWarps + 1];  // 0 = unknown, else 1 + CTAs per SM
     int dev = 0;
     cudaGetDevice(&dev);
-    int cached = cache[dev & 63][wv].load(std::memory_order_relaxed);
+    int cached = smem == 0 ? cache[dev & 63][wv].load(std::memory_order_relaxed) : 0;
     if (cached == 0) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out, kUnroll, kTG, kA16>,
-                                                          32 * wv, 0) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out, kUnroll, kTG, kMode>,
+                                                          32 * wv, smem) != cudaSuccess) {
             cudaGetLastError();
             per_sm = 0;
         }
         cached = per_sm + 1;
-        cache[dev & 63][wv].store(cached, std::memory_order_relaxed);
+        if (smem == 0) cache[dev & 63][wv].store(cached, std::memory_order_relaxed);
     }
     return cached - 1;
 }
@@ -334,15 +408,15 @@ int ctas_per_sm(int wv) {
 // evenly to within 10% (every warp finishes at about the same time) and for
 // which the whole grid is resident in one wave, the one with the most weight
 // bytes in flight (capped where HBM saturates, ~20 MB on GB300); 0 if none.
-template <bool kF32Out, int kUnroll, int kTG, bool kA16 = false>
-int pick_warps(int64_t ctas, int KB, int num_sms, int64_t* inflight_out) {
+template <bool kF32Out, int kUnroll, int kTG, int kMode = kModeW8A8>
+int pick_warps(int64_t ctas, int KB, int num_sms, int64_t* inflight_out, size_t smem = 0) {
     constexpr int64_t kSaturate = int64_t(20) << 20;
     int best = 0;
     int64_t best_inflight = -1;
     for (int wv = 1; wv <= kMaxWarps && wv <= KB; ++wv) {
         const int per_warp = (KB + wv - 1) / wv;
         if (10 * KB < 9 * wv * per_warp) continue;  // warps would finish more than 10% apart
-        if (ctas > static_cast<int64_t>(ctas_per_sm<kF32Out, kUnroll, kTG, kA16>(wv)) * num_sms) continue;
+        if (ctas > static_cast<int64_t>(ctas_per_sm<kF32Out, kUnroll, kTG, kMode>(wv, smem)) * num_sms) continue;
         int64_t inflight = ctas * wv * (per_warp < kUnroll ? per_warp : kUnroll) * (16 * kGroup);
         if (inflight > kSaturate) inflight = kSaturate;
         if (inflight > best_inflight || (inflight == best_inflight && wv < best)) {
@@ -354,7 +428,7 @@ int pick_warps(int64_t ctas, int KB, int num_sms, int64_t* inflight_out) {
     return best;
 }
 
-template <bool kF32Out, int kUnroll, int kTG, bool kA16 = false>
+template <bool kF32Out, int kUnroll, int kTG, int kMode = kModeW8A8>
 cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N, int K,
                          void* out, int num_sms, cudaStream_t stream) {
     const int KB = K / kGroup;
@@ -362,16 +436,32 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
     const int64_t ctas = static_cast<int64_t>(grid.x) * grid.y;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    int wv = pick_warps<kF32Out, kUnroll, kTG, kA16>(ctas, KB, num_sms, nullptr);
+    // The fused mode keeps min(8, M) rows of codes and scales in dynamic shared memory.
+    const size_t smem = kMode == kModeFQ ? fused_smem_bytes(M, K) : 0;
+    if constexpr (kMode == kModeFQ) {
+        static std::atomic<uint64_t> configured{0};  // one bit per device
+        int dev = 0;
+        cudaGetDevice(&dev);
+        const uint64_t bit = 1ull << (dev & 63);
+        if (!(configured.load(std::memory_order_acquire) & bit)) {
+            const cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<kF32Out, kUnroll, kTG, kMode>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(kFusedMaxSmem));
+            if (e != cudaSuccess) return e;
+            configured.fetch_or(bit, std::memory_order_release);
+        }
+    }
+    int wv = pick_warps<kF32Out, kUnroll, kTG, kMode>(ctas, KB, num_sms, nullptr, smem);
     if (wv == 0) wv = KB < 4 ? KB : 4;  // grid larger than one wave: plain 4-warp CTAs
     cfg.blockDim = dim3(32 * wv);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<kF32Out, kUnroll, kTG, kA16>, q, sa, w, sw, M, N, K, out);
+    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<kF32Out, kUnroll, kTG, kMode>, q, sa, w, sw, M, N, K, out);
 }
 
 }  // namespace
@@ -414,10 +504,10 @@ cudaError_t launch_gemm_w8a16(const void* x, const uint8_t* w, const float* sw, 
     // each SM keeps in flight. Depth 1 measured fastest at M = 1, 8 and 16.
     const uint8_t* xb = static_cast<const uint8_t*>(x);
     if (M > 8)  // two token groups per CTA share the widened weights
-        return out_f32 ? launch_typed<true, 1, 2, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
-                       : launch_typed<false, 1, 2, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
-    return out_f32 ? launch_typed<true, 1, 1, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
-                   : launch_typed<false, 1, 1, true>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
+        return out_f32 ? launch_typed<true, 1, 2, kModeA16>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
+                       : launch_typed<false, 1, 2, kModeA16>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
+    return out_f32 ? launch_typed<true, 1, 1, kModeA16>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
+                   : launch_typed<false, 1, 1, kModeA16>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
 }
 
 cudaError_t launch_gemm_skinny_grouped(const GemmProblem* probs, int count, bool out_f32, cudaStream_t stream) {
@@ -470,6 +560,20 @@ cudaError_t launch_gemm_skinny_grouped(const GemmProblem* probs, int count, bool
     cfg.numAttrs = 1;
     return out_f32 ? cudaLaunchKernelEx(&cfg, gemm_skinny_grouped_kernel<true, 1>, args)
                    : cudaLaunchKernelEx(&cfg, gemm_skinny_grouped_kernel<false, 1>, args);
+}
+
+bool fused_fits(int M, int K) { return fused_smem_bytes(M, K) <= kFusedMaxSmem; }
+
+cudaError_t launch_linear_fused(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
+                                bool out_f32, int num_sms, cudaStream_t stream) {
+    // The W8A8 loop with the same load depth rule as launch_gemm_skinny, so
+    // that at equal launch geometry the two paths sum in the same order.
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    if (K / kGroup >= 32)
+        return out_f32 ? launch_typed<true, 1, 1, kModeFQ>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
+                       : launch_typed<false, 1, 1, kModeFQ>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
+    return out_f32 ? launch_typed<true, 4, 1, kModeFQ>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
+                   : launch_typed<false, 4, 1, kModeFQ>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
 }
 
 }  // namespace fp8act

@@ -8,6 +8,7 @@
 // dual-L20 Qwen3.8-27B-FP8 tuning report (section 8); the pages do not spell
 // out the arithmetic, and the rule above is the plain reading of an amax/448
 // fp32 scale.
+#include "act_group.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100_ptx.cuh"
@@ -89,23 +90,10 @@ __device__ __forceinline__ void act_quant_body(const Map& map, int64_t groups) {
 #pragma unroll
         for (int u = 0; u < kActUnroll; ++u) {
             const int64_t g = base + 2 * u + half;
-            float f[8];
-            f[0] = bf16_lo(v[u].x); f[1] = bf16_hi(v[u].x);
-            f[2] = bf16_lo(v[u].y); f[3] = bf16_hi(v[u].y);
-            f[4] = bf16_lo(v[u].z); f[5] = bf16_hi(v[u].z);
-            f[6] = bf16_lo(v[u].w); f[7] = bf16_hi(v[u].w);
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-            for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, kE4M3Max);
-            uint32_t c[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+            uint2 codes;
+            const float s = quant_group_halfwarp(v[u], codes);
             if (g < groups) {
-                qg[u][hl] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+                qg[u][hl] = codes;
                 if (hl == 0) *sg[u] = s;
             }
         }

@@ -55,6 +55,8 @@ def load(build: bool = False) -> ctypes.CDLL:
     L.fp8_block_gemm_f32.argtypes = [p, p, p, p, i, i, i, p, p]
     L.fp8_block_gemm_w8a16.argtypes = [p, p, p, i, i, i, p, p]
     L.fp8_block_gemm_w8a16_f32.argtypes = [p, p, p, i, i, i, p, p]
+    L.fp8_linear.argtypes = [p, p, p, i, i, i, p, p]
+    L.fp8_linear_f32.argtypes = [p, p, p, i, i, i, p, p]
     L.fp8_act_quant_grouped.argtypes = [p, i, p]
     L.fp8_block_gemm_grouped.argtypes = [p, i, p]
     L.fp8_block_gemm_grouped_f32.argtypes = [p, i, p]
@@ -64,6 +66,7 @@ def load(build: bool = False) -> ctypes.CDLL:
     for fn in (L.fp8_act_quant, L.fp8_weight_quant, L.fp8_block_gemm, L.fp8_block_gemm_f32,
                L.fp8_block_gemm_w8a16, L.fp8_block_gemm_w8a16_f32,
                L.fp8_act_quant_grouped, L.fp8_block_gemm_grouped, L.fp8_block_gemm_grouped_f32,
+               L.fp8_linear, L.fp8_linear_f32,
                L.fp8act_check_status, L.fp8act_version):
         fn.restype = ctypes.c_int
     _lib = L
@@ -152,6 +155,16 @@ def fp8_block_gemm(q, sa, w, sw, out=None, stream=None) -> torch.Tensor:
 def fp8_block_gemm_f32(q, sa, w, sw, out=None, stream=None) -> torch.Tensor:
     """fp32 [M, N] output of the same kernels (no bf16 cast)."""
     return _gemm("fp8_block_gemm_f32", torch.float32, q, sa, w, sw, out, stream)
+
+
+def fp8_linear(x, w, sw, out=None, stream=None) -> torch.Tensor:
+    """bf16 [M, N] = fp8_block_gemm(fp8_act_quant(x), w, sw) in one launch (decode-sized M)."""
+    return _gemm_w8a16("fp8_linear", torch.bfloat16, x, w, sw, out, stream)
+
+
+def fp8_linear_f32(x, w, sw, out=None, stream=None) -> torch.Tensor:
+    """fp32 [M, N] output of the fused kernels (no bf16 cast)."""
+    return _gemm_w8a16("fp8_linear_f32", torch.float32, x, w, sw, out, stream)
 
 
 def _gemm_w8a16(fn_name: str, out_dtype, x, w, sw, out, stream):

@@ -123,6 +123,29 @@ FP8ACT_API int fp8_block_gemm_w8a16_f32(const void* x_bf16, const void* w_e4m3, 
                                         int K, float* out_f32, void* stream);
 
 /*
+ * Fused linear layer: fp8_act_quant and fp8_block_gemm in one launch,
+ *   out = fp8_block_gemm(fp8_act_quant(x), w, sw),
+ * with the same activation codes and scales bit for bit (the kernel
+ * quantises with the activation kernel's own group code). The
+ * single-RTX-PRO-6000 Qwen3.8-27B post (smartx.com), section "单并发优化",
+ * counts the quantisation launch per linear layer among the costs of the
+ * W8A8 path at one request, and the zskr.cn Qwen3-27B decode article,
+ * section 3.3, fuses the quantisation op into the preceding computation.
+ * Here each CTA of the weight-streaming kernel quantises its (at most 8)
+ * tokens into shared memory before streaming its weights, so every CTA
+ * repeats the activation work: the call is meant for decode (small M).
+ * Needs min(8, M) * (K + K / 32) bytes of shared memory per CTA, at most
+ * 200 KiB (K <= 24576 once M >= 8); larger K returns FP8ACT_ERR_SHAPE.
+ *   x_bf16     : [M, K] bf16 activations (16-byte aligned)
+ *   w_e4m3, sw : weight codes [N, K] and scales [ceil(N/128), K/128]
+ *   out_bf16   : [M, N] bf16 out (out_f32: [M, N] fp32, the value before the cast)
+ */
+FP8ACT_API int fp8_linear(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N, int K,
+                          void* out_bf16, void* stream);
+FP8ACT_API int fp8_linear_f32(const void* x_bf16, const void* w_e4m3, const float* sw, int M, int N, int K,
+                              float* out_f32, void* stream);
+
+/*
  * Grouped calls: several independent problems in one kernel launch.
  * The zskr.cn decode-optimisation article on Qwen3-27B, section 3.3
  * ("第三板斧"), merges the Q, K and V matmuls into one operator to save

@@ -23,6 +23,7 @@ def test_library_exports_every_header_symbol(lib):
     assert {"fp8_act_quant", "fp8_weight_quant", "fp8_block_gemm", "fp8_block_gemm_f32",
             "fp8_block_gemm_w8a16", "fp8_block_gemm_w8a16_f32",
             "fp8_act_quant_grouped", "fp8_block_gemm_grouped", "fp8_block_gemm_grouped_f32",
+            "fp8_linear", "fp8_linear_f32",
             "fp8act_strerror", "fp8act_check_status", "fp8act_version"} <= set(names)
     raw = ctypes.CDLL(fp8act.lib_path())
     for n in names:
@@ -138,3 +139,15 @@ def test_act_quant_grouped_argument_checks(lib):
     assert f(ctypes.byref(arr), 2, None) == ALIGN
     arr = (P * 1)(P(None, None, None, 0, 128))
     assert f(ctypes.byref(arr), 1, None) == OK
+
+
+@pytest.mark.parametrize("name", ["fp8_linear", "fp8_linear_f32"])
+def test_linear_argument_checks(lib, name):
+    f = getattr(lib, name)
+    assert f(A16, A16, A16, 1, 128, 64, A16, None) == SHAPE
+    assert f(A16, A16, A16, -1, 128, 128, A16, None) == SHAPE
+    assert f(A16, A16, A16, 8, 128, 25 * 1024, A16, None) == SHAPE   # 8 rows of K codes exceed 200 KiB
+    assert f(None, None, None, 0, 128, 128, None, None) == OK
+    assert f(A16, None, A16, 1, 128, 128, A16, None) == NULL
+    assert f(A16 + 8, A16, A16, 1, 128, 128, A16, None) == ALIGN
+    assert f(A16, A16, A16 + 2, 1, 128, 128, A16, None) == ALIGN

@@ -284,3 +284,58 @@ def test_gemm_grouped_ragged_mix(fp8act):
     dims = [(17, 128, 1), (200, 256, 5), (1000, 384, 12), (257, 768, 16), (130, 1152, 3), (300, 512, 40)]
     probs = [Problem(N, K, seed=900 + i) for i, (N, K, _) in enumerate(dims)]
     _grouped_compare(fp8act, probs, [m for _, _, m in dims], seed=910)
+
+
+# ------------------------------------------- fused act-quant + GEMM (fp8_linear)
+def _linear_compare(fp8act, p, M, seed, edge=False):
+    from parity_util import compare_gemm
+    x = inputs.edge_activations_bf16(M, p.K, seed) if edge else inputs.activations_bf16(M, p.K, seed)
+    xd = x.cuda()
+    out = fp8act.fp8_linear(xd, p.w, p.sw)
+    out32 = fp8act.fp8_linear_f32(xd, p.w, p.sw)
+    torch.cuda.synchronize()
+    q_ref, sa_ref = oracle.act_quant(inputs.bf16_bits(x))
+    y, aabs, ref = oracle.block_gemm(q_ref, sa_ref, p.w_ref, p.sw_ref)
+    compare_gemm(out, out32, y, aabs, ref, p.K)
+    return xd, out32
+
+
+@pytest.mark.parametrize("si", range(len(SHAPES)))
+@pytest.mark.parametrize("M", [1, 3, 8, 12, 16])
+def test_linear_fused_decode_widths(fp8act, si, M):
+    _linear_compare(fp8act, problem(si), M, seed=600 + M)
+
+
+@pytest.mark.parametrize("si", range(len(SHAPES)))
+def test_linear_fused_equals_two_launches_at_m1(fp8act, si):
+    """At M = 1 the fused kernel runs the two-launch path's launch geometry,
+    so equal codes and scales give the same fp32 sums bit for bit: any code
+    the in-kernel quantisation got wrong would show here."""
+    p = problem(si)
+    xd, out32 = _linear_compare(fp8act, p, 1, seed=650 + si)
+    q, sa = fp8act.fp8_act_quant(xd)
+    ref32 = fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw)
+    torch.cuda.synchronize()
+    assert torch.equal(out32, ref32)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 17, 128), (5, 200, 256), (12, 1000, 384), (2, 257, 9 * 128)])
+def test_linear_fused_ragged(fp8act, M, N, K):
+    from parity_util import Problem
+    _linear_compare(fp8act, Problem(N, K, seed=N + 5 * K), M, seed=M)
+
+
+def test_linear_fused_edge_groups(fp8act):
+    """Edge-case groups (zeros, -0, single values, 2^-126, bf16 subnormals,
+    outliers, E4M3 midpoints, constants). K = 9 groups so that every row
+    holds one group of each kind, as in the W8A8 edge test; at M = 1 the
+    fused result must equal the two-launch one bit for bit."""
+    from parity_util import Problem
+    p = Problem(640, 9 * 128, seed=5)
+    for M in (1, 8, 13):
+        xd, out32 = _linear_compare(fp8act, p, M, seed=M, edge=True)
+        if M == 1:
+            q, sa = fp8act.fp8_act_quant(xd)
+            ref32 = fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw)
+            torch.cuda.synchronize()
+            assert torch.equal(out32, ref32)
