@@ -20,9 +20,10 @@
  * Conventions for every entry point
  * ---------------------------------
  * - Pointers are DEVICE pointers on the current CUDA device, owned by the
- *   caller. The library never allocates, frees or synchronises inside these
- *   calls and reads no device data on the host, so every call can be
- *   captured in a CUDA graph.
+ *   caller (the one exception: the `problems` arrays of the grouped calls
+ *   live in host memory and are read during the call only). The library
+ *   never allocates, frees or synchronises inside these calls and reads no
+ *   device data on the host, so every call can be captured in a CUDA graph.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
  *   enqueued asynchronously; the returned status covers argument checks and
  *   the launch only. Kernel-side timeouts are reported by
@@ -52,7 +53,8 @@ extern "C" {
 typedef enum {
     FP8ACT_OK = 0,
     FP8ACT_ERR_NULL = 1,     /* a required pointer is NULL                         */
-    FP8ACT_ERR_SHAPE = 2,    /* M, N < 0; K <= 0 or K % 128 != 0; size overflow   */
+    FP8ACT_ERR_SHAPE = 2,    /* M, N < 0; K <= 0 or K % 128 != 0; size overflow;
+                                more than 16 grouped problems; fp8_linear K too large */
     FP8ACT_ERR_ALIGN = 3,    /* a pointer violates the alignment rule above       */
     FP8ACT_ERR_LAUNCH = 4,   /* the kernel launch failed (cudaGetLastError)       */
     FP8ACT_ERR_TIMEOUT = 5,  /* a kernel's bounded wait gave up (see check_status) */
