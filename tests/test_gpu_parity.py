@@ -339,3 +339,66 @@ def test_linear_fused_edge_groups(fp8act):
             ref32 = fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw)
             torch.cuda.synchronize()
             assert torch.equal(out32, ref32)
+
+
+# ------------------------------- the newer entry points: graphs, streams, canaries
+def test_new_paths_capture_in_cuda_graph_and_match_eager(fp8act):
+    """W8A16, fused and grouped calls captured in one CUDA graph on a
+    non-default stream give the same bits as the eager calls."""
+    ps = [problem(si) for si in range(len(SHAPES))]
+    xs = [inputs.activations_bf16(3, p.K, seed=960 + i).cuda() for i, p in enumerate(ps)]
+    eager16 = [fp8act.fp8_block_gemm_w8a16(x, p.w, p.sw) for x, p in zip(xs, ps)]
+    eagerf = [fp8act.fp8_linear(x, p.w, p.sw) for x, p in zip(xs, ps)]
+    qsa = fp8act.fp8_act_quant_grouped(xs)
+    eagerg = fp8act.fp8_block_gemm_grouped([(q, sa, p.w, p.sw) for (q, sa), p in zip(qsa, ps)])
+    torch.cuda.synchronize()
+    o16 = [torch.empty_like(t) for t in eager16]
+    of = [torch.empty_like(t) for t in eagerf]
+    og = [torch.empty_like(t) for t in eagerg]
+    qsa2 = [(torch.empty_like(q), torch.empty_like(sa)) for q, sa in qsa]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for x, p, o in zip(xs, ps, o16):
+                fp8act.fp8_block_gemm_w8a16(x, p.w, p.sw, out=o, stream=s)
+            for x, p, o in zip(xs, ps, of):
+                fp8act.fp8_linear(x, p.w, p.sw, out=o, stream=s)
+            fp8act.fp8_act_quant_grouped(xs, outs=qsa2, stream=s)
+            fp8act.fp8_block_gemm_grouped([(q, sa, p.w, p.sw) for (q, sa), p in zip(qsa2, ps)], outs=og, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager16 + eagerf + eagerg, o16 + of + og):
+        assert torch.equal(a, b)
+
+
+def test_new_paths_write_nothing_outside_out(fp8act):
+    p = problem(1)
+    pad = 4096
+    for M in (1, 7, 13):
+        x = inputs.activations_bf16(M, p.K, seed=M).cuda()
+        q, sa = fp8act.fp8_act_quant(x)
+        for call in ("w8a16", "fused", "grouped"):
+            buf = torch.full((M * p.N + 2 * pad,), -7.0, dtype=torch.bfloat16, device="cuda")
+            out = buf[pad:pad + M * p.N].view(M, p.N)
+            if call == "w8a16":
+                fp8act.fp8_block_gemm_w8a16(x, p.w, p.sw, out=out)
+            elif call == "fused":
+                fp8act.fp8_linear(x, p.w, p.sw, out=out)
+            else:
+                fp8act.fp8_block_gemm_grouped([(q, sa, p.w, p.sw)], outs=[out])
+            torch.cuda.synchronize()
+            assert torch.all(buf[:pad] == -7.0) and torch.all(buf[pad + M * p.N:] == -7.0), (call, M)
+
+
+def test_fused_at_its_shared_memory_limit(fp8act):
+    """M = 8 and K = 24576: 8 rows of codes and scales take 198 KiB of the
+    fused kernel's 200 KiB; one more K group is refused on the host."""
+    from parity_util import Problem
+    p = Problem(256, 24576, seed=17)
+    _linear_compare(fp8act, p, 8, seed=18)
+    x = torch.zeros((8, 24576 + 1024), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((256, 24576 + 1024), dtype=torch.uint8, device="cuda")
+    sw = torch.ones((2, (24576 + 1024) // 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(fp8act.Fp8ActError):
+        fp8act.fp8_linear(x, w, sw)
