@@ -14,6 +14,8 @@ Printed JSON line (rank 0):
              steps replayed as CUDA graphs, inputs resident in HBM
   e2e        the same through the public API with the activations copied in
              from pinned host memory and the outputs copied back every step
+             (calls captured once and replayed as a CUDA graph; the eagerly
+             issued figure is reported beside it)
   roofline   the block GEMM kernel against the measured HBM copy bandwidth
   cpu_baseline  the CPU oracle on the same workload (host cores)
   sweep      us/call per shape at M = 1..8 (the no-cliff check), 64, 102
@@ -231,16 +233,26 @@ class Workload:
         self.shapes = weights.shapes
         self.copies = weights.copies
         self.w, self.sw = weights.w, weights.sw
+        # The activations of all shapes live in one device buffer (and one pinned
+        # host buffer), the outputs in another, so that the end-to-end leg moves
+        # each direction with a single copy. Every slice starts on a 256-byte
+        # boundary (M * K * 2 and M * N * 2 are multiples of 256).
+        self.x_all = torch.empty(sum(M * K for _, K in self.shapes), dtype=torch.bfloat16, device=device)
+        self.out_all = torch.empty(sum(M * N for N, _ in self.shapes), dtype=torch.bfloat16, device=device)
+        self.x_host_all = torch.empty(self.x_all.numel(), dtype=torch.bfloat16).pin_memory()
+        self.out_host_all = torch.empty(self.out_all.numel(), dtype=torch.bfloat16).pin_memory()
         self.x, self.q, self.sa, self.out = [], [], [], []
-        self.x_host, self.out_host = [], []
+        xo = oo = 0
         for si, (N, K) in enumerate(self.shapes):
             x = inputs.activations_bf16(M, K, inputs.activation_seed(si, 0))
-            self.x_host.append(x.pin_memory())
-            self.x.append(x.to(device))
+            self.x_host_all[xo:xo + M * K].copy_(x.reshape(-1))
+            self.x.append(self.x_all[xo:xo + M * K].view(M, K))
             self.q.append(torch.empty((M, K), dtype=torch.uint8, device=device))
             self.sa.append(torch.empty((M, K // G), dtype=torch.float32, device=device))
-            self.out.append(torch.empty((M, N), dtype=torch.bfloat16, device=device))
-            self.out_host.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
+            self.out.append(self.out_all[oo:oo + M * N].view(M, N))
+            xo += M * K
+            oo += M * N
+        self.x_all.copy_(self.x_host_all)
         torch.cuda.synchronize()
 
     def gemm_bytes_of(self, N: int, K: int) -> int:
@@ -378,7 +390,7 @@ def dist_setup():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+    elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -516,28 +528,36 @@ def main() -> None:
 
     # ---- e2e: public API, activations from pinned host, outputs back, every step
     def e2e_step(c):
-        for si in range(len(wl.shapes)):
-            wl.x[si].copy_(wl.x_host[si], non_blocking=True)
+        wl.x_all.copy_(wl.x_host_all, non_blocking=True)
         wl.enqueue_step(c, stream)
-        for si in range(len(wl.shapes)):
-            wl.out_host[si].copy_(wl.out[si], non_blocking=True)
+        wl.out_host_all.copy_(wl.out_all, non_blocking=True)
     e2e_steps = 0 if args.no_e2e else max(50, args.steps // 10)
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            e2e_step(i % wl.copies)
-        torch.cuda.synchronize()
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0 = time.perf_counter()
-        s0.record(stream)
-        for i in range(e2e_steps):
-            e2e_step(i % wl.copies)
-        s1.record(stream)
-        s1.synchronize()
-        wall = (time.perf_counter() - t0) / max(e2e_steps, 1)
-    t_e2e = max(s0.elapsed_time(s1) / 1e3 / max(e2e_steps, 1), wall)
-    t_e2e = max_over_ranks(world, t_e2e)
-    h2d = sum(x.numel() * 2 for x in wl.x_host)
-    d2h = sum(o.numel() * 2 for o in wl.out_host)
+
+    def timed_e2e(run) -> float:
+        """Seconds per step of `run(i)` over e2e_steps steps: the larger of the
+        CUDA-event time on the stream and the host wall time."""
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                run(i)
+            torch.cuda.synchronize()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            s0.record(stream)
+            for i in range(e2e_steps):
+                run(i)
+            s1.record(stream)
+            s1.synchronize()
+            wall = (time.perf_counter() - t0) / max(e2e_steps, 1)
+        return max(s0.elapsed_time(s1) / 1e3 / max(e2e_steps, 1), wall)
+
+    # Eager: every API call issued from Python each step (binding overhead included).
+    t_e2e_eager = max_over_ranks(world, timed_e2e(lambda i: e2e_step(i % wl.copies)))
+    # Graph: the same calls (copies included) captured once and replayed per step.
+    e2e_graphs = [capture(lambda c=c: e2e_step(c), stream) for c in range(wl.copies)]
+    t_e2e = max_over_ranks(world, timed_e2e(lambda i: e2e_graphs[i % wl.copies].replay()))
+    del e2e_graphs
+    h2d = wl.x_host_all.numel() * 2
+    d2h = wl.out_host_all.numel() * 2
 
     units = wl.gemm_units()
     gemm_bytes = [u[1] for u in units]
@@ -586,7 +606,14 @@ def main() -> None:
                      "us_per_launch": round(sum(gemm_ts) / len(gemm_ts) * 1e6, 3)},
         "e2e": {"value": round(world * (step_flops / 1e12 if bound == "tensor" else step_bytes / 1e9) / t_e2e, 2),
                 "unit": unit,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 5)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 5),
+                "how": "each step: one H2D copy of all activations from pinned host memory, the step's API "
+                       "calls, one D2H copy of all outputs; captured once through the public API and "
+                       "replayed as a CUDA graph per step",
+                "eager": {"value": round(world * (step_flops / 1e12 if bound == "tensor" else step_bytes / 1e9)
+                                         / t_e2e_eager, 2),
+                          "ms_per_step": round(t_e2e_eager * 1e3, 5),
+                          "how": "the same calls issued from Python every step (ctypes binding overhead included)"}},
         "clocks": clk.summary(),
     }
     if not args.no_sweep and rank == 0 and args.workload == "decode":
