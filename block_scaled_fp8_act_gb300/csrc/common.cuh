@@ -36,6 +36,21 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return v;
 }
 
+// 32-byte load of data read exactly once (one 256-bit access; `p` must be
+// 32-byte aligned): bytes 0..15 to lo, 16..31 to hi.
+__device__ __forceinline__ void ld_stream_v8(const void* p, uint4& lo, uint4& hi) {
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+        : "l"(p));
+}
+
+// 32-byte load of data that many CTAs re-read (kept in L1); `p` 32-byte aligned.
+__device__ __forceinline__ void ld_ro_v8(const void* p, uint4& lo, uint4& hi) {
+    asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+        : "l"(p));
+}
+
 // 8-byte load of data read exactly once.
 __device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
     uint2 v;

@@ -51,11 +51,11 @@
 // memory with the activation kernel's own group code (so the codes and
 // scales are the same bits), then runs the W8A8 loop on them. Every CTA
 // repeats the quantisation of the same tokens, so the mode suits small M.
-#include "act_group.cuh"
 #include <atomic>
 
 #include <cuda_fp16.h>
 
+#include "act_group.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100_ptx.cuh"
@@ -70,6 +70,12 @@ constexpr int kMaxWarps = 16;
 constexpr int kModeW8A8 = 0;
 constexpr int kModeA16 = 1;
 constexpr int kModeFQ = 2;
+// Added to kModeW8A8 / kModeFQ: each lane streams 32 contiguous bytes of a
+// weight row per block with one 256-bit load (needs 32-byte aligned weights
+// and codes) instead of two 16-byte chunks 64 bytes apart.
+constexpr int kWideBit = 4;
+constexpr int base_mode(int mode) { return mode & 3; }
+constexpr bool wide_mode(int mode) { return (mode & kWideBit) != 0; }
 constexpr size_t kFusedMaxSmem = 200 * 1024;  // the fused mode's shared-memory ceiling per CTA
 // L2 prefetch distance, in warp steps: each warp keeps the weight lines of
 // the next steps on their way into L2 (prefetches hold no registers). One
@@ -130,7 +136,7 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                                             const uint8_t* __restrict__ w, const float* __restrict__ sw, int M,
                                             int N, int K, void* __restrict__ out, int n0, int m0,
                                             float (*red)[16][8 * kTG], uint8_t* fq_smem = nullptr) {
-    static_assert(kMode != kModeFQ || kTG == 1, "the fused mode quantises one group of 8 tokens per CTA");
+    static_assert(base_mode(kMode) != kModeFQ || kTG == 1, "the fused mode quantises one group of 8 tokens per CTA");
     const int KB = K / kGroup;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -140,8 +146,15 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
 
     const bool ok_r0 = n0 + g < N;
     const bool ok_r1 = n0 + g + 8 < N;
-    const uint8_t* w_r0 = w + static_cast<int64_t>(n0 + g) * K + 16 * t;
-    const uint8_t* w_r1 = w + static_cast<int64_t>(n0 + g + 8) * K + 16 * t;
+    constexpr bool kWide = wide_mode(kMode);
+    static_assert(!kWide || base_mode(kMode) != kModeA16, "the weight-only mode keeps 16-byte chunks");
+    // Lane (g, t) takes bytes [16t, 16t+16) and [64+16t, 64+16t+16) of each
+    // 128-byte block, or with kWide the 32 contiguous bytes [32t, 32t+32).
+    // Either way the K positions depend on t only, the same for every weight
+    // row and token, so A and B fragments pair up the same K elements.
+    const int lane_off = kWide ? 32 * t : 16 * t;
+    const uint8_t* w_r0 = w + static_cast<int64_t>(n0 + g) * K + lane_off;
+    const uint8_t* w_r1 = w + static_cast<int64_t>(n0 + g + 8) * K + lane_off;
     const float* sw_r = sw + static_cast<int64_t>(n0 / kGroup) * KB;
 
     float acc[kTG][4];
@@ -161,7 +174,7 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
     const uint8_t* w_pf = w + static_cast<int64_t>(n0 + lane) * K;
     if (pf_lane) {
 #pragma unroll
-        for (int s = kMode == kModeFQ ? 0 : 1; s <= kL2Ahead; ++s)
+        for (int s = base_mode(kMode) == kModeFQ ? 0 : 1; s <= kL2Ahead; ++s)
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int kb = warp + s * stride + u * nwarps;
@@ -172,7 +185,7 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
     const int fq_rows = M - m0 < 8 ? M - m0 : 8;
     const uint8_t* q_s = fq_smem;
     const float* sa_s = reinterpret_cast<const float*>(fq_smem + static_cast<int64_t>(fq_rows) * K);
-    if constexpr (kMode == kModeFQ) {
+    if constexpr (base_mode(kMode) == kModeFQ) {
         // Quantise this CTA's tokens m0 .. m0 + fq_rows - 1 into shared memory:
         // half-warp h of warp w takes groups 2 w + h, 2 w + h + 2 nwarps, ...
         // (row-major over (token, K group)); the whole warp runs every pass
@@ -214,16 +227,22 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
             const int kb = kb0 + u * nwarps;
             const bool ok_k = kb < KB;
             const int64_t off = static_cast<int64_t>(kb) * kGroup;
-            r0lo[u] = (ok_k && ok_r0) ? ld_stream_v4(w_r0 + off) : zero;
-            r0hi[u] = (ok_k && ok_r0) ? ld_stream_v4(w_r0 + off + 64) : zero;
-            r1lo[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off) : zero;
-            r1hi[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off + 64) : zero;
+            if constexpr (kWide) {
+                r0lo[u] = r0hi[u] = r1lo[u] = r1hi[u] = zero;
+                if (ok_k && ok_r0) ld_stream_v8(w_r0 + off, r0lo[u], r0hi[u]);
+                if (ok_k && ok_r1) ld_stream_v8(w_r1 + off, r1lo[u], r1hi[u]);
+            } else {
+                r0lo[u] = (ok_k && ok_r0) ? ld_stream_v4(w_r0 + off) : zero;
+                r0hi[u] = (ok_k && ok_r0) ? ld_stream_v4(w_r0 + off + 64) : zero;
+                r1lo[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off) : zero;
+                r1hi[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off + 64) : zero;
+            }
         }
         if (!waited) {
             ptx::griddep_wait();
             waited = true;
         }
-        if constexpr (kMode == kModeA16) {
+        if constexpr (base_mode(kMode) == kModeA16) {
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int kb = kb0 + u * nwarps;
@@ -263,8 +282,9 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
             for (int j = 0; j < kTG; ++j) {
                 const int m = m0 + 8 * j + g;  // this lane's token for the B fragment
                 const bool ok_x = m < M;
-                const uint8_t* x_r = kMode == kModeFQ ? q_s + static_cast<int64_t>(g) * K + 16 * t
-                                                      : q + static_cast<int64_t>(m) * K + 16 * t;
+                const uint8_t* x_r = base_mode(kMode) == kModeFQ ? q_s + static_cast<int64_t>(g) * K + lane_off
+                                                                 : q + static_cast<int64_t>(m) * K + lane_off;
+                constexpr int kHiOff = kWide ? 16 : 64;  // byte offset of the lane's second 16 bytes
                 const int c0 = m0 + 8 * j + 2 * t;  // token columns of this lane's accumulators
                 uint4 xlo[kUnroll], xhi[kUnroll];
 #pragma unroll
@@ -272,9 +292,12 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                     const int kb = kb0 + u * nwarps;
                     const bool ok_k = kb < KB;
                     const int64_t off = static_cast<int64_t>(kb) * kGroup;
-                    if constexpr (kMode == kModeFQ) {
+                    if constexpr (base_mode(kMode) == kModeFQ) {
                         xlo[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + off) : zero;
-                        xhi[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + off + 64) : zero;
+                        xhi[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + off + kHiOff) : zero;
+                    } else if constexpr (kWide) {
+                        xlo[u] = xhi[u] = zero;
+                        if (ok_k && ok_x) ld_ro_v8(x_r + off, xlo[u], xhi[u]);
                     } else {
                         xlo[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off) : zero;
                         xhi[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off + 64) : zero;
@@ -291,7 +314,7 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                         mma_e4m3_16x8x32(d, r0hi[u].z, r1hi[u].z, r0hi[u].w, r1hi[u].w, xhi[u].z, xhi[u].w);
                         const float s_w = __ldg(sw_r + kb);
                         float sa0 = 0.f, sa1 = 0.f;
-                        if constexpr (kMode == kModeFQ) {
+                        if constexpr (base_mode(kMode) == kModeFQ) {
                             if (c0 < M) sa0 = sa_s[(c0 - m0) * KB + kb];
                             if (c0 + 1 < M) sa1 = sa_s[(c0 + 1 - m0) * KB + kb];
                         } else {
@@ -437,8 +460,8 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     // The fused mode keeps min(8, M) rows of codes and scales in dynamic shared memory.
-    const size_t smem = kMode == kModeFQ ? fused_smem_bytes(M, K) : 0;
-    if constexpr (kMode == kModeFQ) {
+    const size_t smem = base_mode(kMode) == kModeFQ ? fused_smem_bytes(M, K) : 0;
+    if constexpr (base_mode(kMode) == kModeFQ) {
         static std::atomic<uint64_t> configured{0};  // one bit per device
         int dev = 0;
         cudaGetDevice(&dev);
@@ -472,9 +495,21 @@ cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const u
     // Above M = 8 the grid gets one row of CTAs per 8 tokens (each re-reads
     // the weights, mostly from L2); for 9..16 tokens this measured faster than
     // CTAs that hold 16 tokens against one weight fragment.
-    if (unroll >= 4)
+    // 256-bit weight and code loads on the depth-4 (short K) path when both
+    // start on 32-byte boundaries (rows are K bytes apart, K a multiple of
+    // 128, so every lane's 32-byte chunk then is aligned too; the API
+    // guarantees only 16). Measured: 3.8 against 4.1 us on (5120, 3072) at
+    // M = 1; on the depth-1 path they were slower (16.2 against 14.6 us on
+    // (17408, 5120)), so it keeps 16-byte chunks.
+    constexpr int kW = kModeW8A8 | kWideBit;
+    const bool wide = ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(w)) & 31) == 0;
+    if (unroll >= 4) {
+        if (wide)
+            return out_f32 ? launch_typed<true, 4, 1, kW>(q, sa, w, sw, M, N, K, out, num_sms, stream)
+                           : launch_typed<false, 4, 1, kW>(q, sa, w, sw, M, N, K, out, num_sms, stream);
         return out_f32 ? launch_typed<true, 4, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream)
                        : launch_typed<false, 4, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream);
+    }
     if (unroll >= 2)
         return out_f32 ? launch_typed<true, 2, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream)
                        : launch_typed<false, 2, 1>(q, sa, w, sw, M, N, K, out, num_sms, stream);
@@ -568,10 +603,19 @@ cudaError_t launch_linear_fused(const void* x, const uint8_t* w, const float* sw
                                 bool out_f32, int num_sms, cudaStream_t stream) {
     // The W8A8 loop with the same load depth rule as launch_gemm_skinny, so
     // that at equal launch geometry the two paths sum in the same order.
+    // 256-bit weight loads on the depth-4 path as in launch_gemm_skinny_unroll
+    // (the codes come from shared memory here, so only the weights' alignment
+    // matters).
     const uint8_t* xb = static_cast<const uint8_t*>(x);
-    if (K / kGroup >= 32)
+    constexpr int kW = kModeFQ | kWideBit;
+    const bool wide = (reinterpret_cast<uintptr_t>(w) & 31) == 0;
+    if (K / kGroup >= 32) {
         return out_f32 ? launch_typed<true, 1, 1, kModeFQ>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
                        : launch_typed<false, 1, 1, kModeFQ>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
+    }
+    if (wide)
+        return out_f32 ? launch_typed<true, 4, 1, kW>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
+                       : launch_typed<false, 4, 1, kW>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
     return out_f32 ? launch_typed<true, 4, 1, kModeFQ>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream)
                    : launch_typed<false, 4, 1, kModeFQ>(xb, nullptr, w, sw, M, N, K, out, num_sms, stream);
 }

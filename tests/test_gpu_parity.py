@@ -402,3 +402,23 @@ def test_fused_at_its_shared_memory_limit(fp8act):
     sw = torch.ones((2, (24576 + 1024) // 128), dtype=torch.float32, device="cuda")
     with pytest.raises(fp8act.Fp8ActError):
         fp8act.fp8_linear(x, w, sw)
+
+
+@pytest.mark.parametrize("si", [1, 0])
+def test_gemm_with_only_16_byte_aligned_operands(fp8act, si):
+    """Codes and weights that start 16 bytes past a 32-byte boundary (the API
+    asks for 16) take the 16-byte-load kernels; the result must still match."""
+    from parity_util import compare_gemm
+    p = problem(si)
+    M = 3
+    q, sa, q_ref, sa_ref = p.activations(M, seed=77)
+    qb = torch.empty(M * p.K + 16, dtype=torch.uint8, device="cuda")[16:].view(M, p.K)
+    qb.copy_(q)
+    wb = torch.empty(p.N * p.K + 16, dtype=torch.uint8, device="cuda")[16:].view(p.N, p.K)
+    wb.copy_(p.w)
+    assert qb.data_ptr() % 32 == 16 and wb.data_ptr() % 32 == 16
+    out = fp8act.fp8_block_gemm(qb, sa, wb, p.sw)
+    out32 = fp8act.fp8_block_gemm_f32(qb, sa, wb, p.sw)
+    torch.cuda.synchronize()
+    y, aabs, ref = oracle.block_gemm(q_ref, sa_ref, p.w_ref, p.sw_ref)
+    compare_gemm(out, out32, y, aabs, ref, p.K)
