@@ -332,23 +332,38 @@ def time_graphs(graphs, steps: int, warmup: int, stream) -> float:
     return start.elapsed_time(end) / 1e3 / steps
 
 
-def gemm_kernel_times(wl: Workload, stream, launches: int = 60, reps: int = 5) -> list[float]:
-    """Average duration (s) of each GEMM launch of a step (one per shape, or
-    one grouped launch): a CUDA graph of `launches` back-to-back calls over the
-    rotating weight copies, timed with events on the launching stream, median
-    over `reps` replays."""
+def chain_times(fns, stream, launches: int, reps: int) -> list[tuple[float, float, float]]:
+    """Per function: (median, p10, p90) seconds per call over `reps` replays of
+    a CUDA graph of `launches` back-to-back calls fn(i) (i = call index),
+    timed with events on the launching stream."""
     out = []
-    for unit in wl.gemm_units():
-        def chain(fn=unit[3]):
+    for fn in fns:
+        def chain(fn=fn):
             for i in range(launches):
-                fn(i % wl.copies, stream)
+                fn(i)
         g = capture(chain, stream)
-        ts = []
-        for _ in range(reps):
-            ts.append(time_graphs([g], 1, 1, stream) / launches)
-        out.append(statistics.median(ts))
+        ts = [time_graphs([g], 1, 1, stream) / launches for _ in range(reps)]
+        out.append((statistics.median(ts), float(np.percentile(ts, 10)), float(np.percentile(ts, 90))))
         del g
     return out
+
+
+def gemm_kernel_times(wl: Workload, stream, launches: int = 60, reps: int = 7, spread=None) -> list[float]:
+    """Average duration (s) of each GEMM launch of a step (one per shape, or
+    one grouped launch) over the rotating weight copies: the median of `reps`
+    replays (p10 / p90 appended to `spread` when given)."""
+    res = chain_times([lambda i, fn=u[3]: fn(i % wl.copies, stream) for u in wl.gemm_units()], stream, launches,
+                      reps)
+    if spread is not None:
+        spread.extend((lo, hi) for _, lo, hi in res)
+    return [med for med, _, _ in res]
+
+
+def quant_kernel_times(wl: Workload, stream, launches: int = 60, reps: int = 7) -> list[tuple[float, float, float]]:
+    """The activation-quantisation launch of each shape, timed like the GEMMs."""
+    from block_scaled_fp8_act_gb300 import fp8act
+    return chain_times([lambda i, si=si: fp8act.fp8_act_quant(wl.x[si], wl.q[si], wl.sa[si], stream=stream)
+                        for si in range(len(wl.shapes))], stream, launches, reps)
 
 
 # ----------------------------------------------------------- CPU oracle leg
@@ -375,10 +390,22 @@ def oracle_step_time(budget_s: float = 12.0) -> dict:
         t_total += dt
     step_bytes = sum(algorithmic_gemm_bytes(1, N, K) + algorithmic_quant_bytes(1, K) for N, K in inputs.SHAPES)
     per_step = statistics.median(times)
-    return {"value": step_bytes / per_step / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+    # one more step on a single thread, for the per-core figure
+    cores = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        for x, w, sw in prepared:
+            q, sa = oracle.act_quant(x)
+            oracle.block_gemm(q, sa, w, sw)
+        single = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": step_bytes / per_step / 1e9, "unit": "GB/s", "cores": cores,
             "kind": "oracle", "seconds_per_step": per_step, "steps_timed": len(times),
+            "single_thread_value": step_bytes / single / 1e9,
             "sample": f"{len(times)} full decode steps (M=1, all five shapes: act quant + exact int64/fp64 GEMM); "
-                      f"weight quantisation untimed"}
+                      f"weight quantisation untimed; single_thread_value from one more step on one thread"}
 
 
 # ----------------------------------------------------------------- runner
@@ -405,7 +432,8 @@ def max_over_ranks(world: int, v: float) -> float:
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -564,7 +592,8 @@ def main() -> None:
         barrier(world)
         t_step = start.elapsed_time(end) / 1e3 / args.steps
         # dominant kernel: the block GEMM, timed per shape on the same stream
-        gemm_ts = gemm_kernel_times(wl, stream, launches=60 if M <= 128 else 8)
+        gemm_spread = []
+        gemm_ts = gemm_kernel_times(wl, stream, launches=60 if M <= 128 else 8, spread=gemm_spread)
     t_step = max_over_ranks(world, t_step)
     step_bytes = wl.step_bytes()
     step_flops = sum(2.0 * M * N * K for N, K in wl.shapes)
@@ -619,18 +648,27 @@ def main() -> None:
         peak_kind = (f"{peaks_kind} bf16 dense (cuBLAS, sustained under the power cap) x {FP8_OVER_BF16:g}, "
                      "the nominal FP8/bf16 ratio")
         roof_unit, per_launch = "TFLOP/s", {"flops_per_launch": sum(gemm_flops) / len(gemm_flops)}
-        per_shape = [{**_label(lb), "us_per_call": round(t * 1e6, 3), "tflops": round(f / t / 1e12, 1),
+        per_shape = [{**_label(lb), "us_per_call": round(t * 1e6, 3), "us_p10": round(lo * 1e6, 3),
+                      "us_p90": round(hi * 1e6, 3), "tflops": round(f / t / 1e12, 1),
                       "frac": round(f / t / 1e12 / peak, 4)}
-                     for lb, t, f in zip(labels, gemm_ts, gemm_flops)]
+                     for lb, t, f, (lo, hi) in zip(labels, gemm_ts, gemm_flops, gemm_spread)]
     else:
         achieved = sum(gemm_bytes) / sum(gemm_ts) / 1e9
         peak = float(peaks["hbm_gbs"])
         peak_kind = f"{peaks_kind} HBM copy bandwidth"
         roof_unit, per_launch = "GB/s", {"bytes_per_launch": sum(gemm_bytes) / len(gemm_bytes)}
-        per_shape = [{**_label(lb), "us_per_call": round(t * 1e6, 3), "gbs": round(b / t / 1e9, 1),
+        per_shape = [{**_label(lb), "us_per_call": round(t * 1e6, 3), "us_p10": round(lo * 1e6, 3),
+                      "us_p90": round(hi * 1e6, 3), "gbs": round(b / t / 1e9, 1),
                       "frac": round(b / t / 1e9 / peak, 4)}
-                     for lb, t, b in zip(labels, gemm_ts, gemm_bytes)]
+                     for lb, t, b, (lo, hi) in zip(labels, gemm_ts, gemm_bytes, gemm_spread)]
 
+    # the activation quantisation, reported on its own (HBM bound at large M)
+    act_quant = None
+    if not wl.bf16_in and not wl.grouped:
+        act_quant = [{"K": K, "us_per_call": round(med * 1e6, 3), "us_p10": round(lo * 1e6, 3),
+                      "us_p90": round(hi * 1e6, 3), "gbs": round(algorithmic_quant_bytes(M, K) / med / 1e9, 1),
+                      "frac": round(algorithmic_quant_bytes(M, K) / med / 1e9 / float(peaks["hbm_gbs"]), 4)}
+                     for (_, K), (med, lo, hi) in zip(wl.shapes, quant_kernel_times(wl, stream))]
     del graphs
     torch.cuda.synchronize()
     result = {
@@ -646,6 +684,7 @@ def main() -> None:
                    "graphs": f"each step is one CUDA graph replay ({launches_per_step} kernels)",
                    "parallelism": f"replicas x{world}"},
         "us_per_call": per_shape,
+        "act_quant": act_quant,
         "gpu_launches": args.steps * launches_per_step,
         "roofline": {"bound": bound, "kernel": kernel, "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": roof_unit, "frac": round(achieved / peak, 4),
@@ -669,7 +708,7 @@ def main() -> None:
         result["sweep"] = sweep(weights, device, stream, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         cb = oracle_step_time(budget_s=args.cpu_budget)
-        result["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        result["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "single_thread_value")}
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
