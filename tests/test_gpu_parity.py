@@ -422,3 +422,20 @@ def test_gemm_with_only_16_byte_aligned_operands(fp8act, si):
     torch.cuda.synchronize()
     y, aabs, ref = oracle.block_gemm(q_ref, sa_ref, p.w_ref, p.sw_ref)
     compare_gemm(out, out32, y, aabs, ref, p.K)
+
+
+def test_act_quant_bit_exact_over_many_scales(fp8act):
+    """17.8M activations whose 1x128 groups are scaled by random factors
+    2^-30 .. 2^30 (so the group scales, their reciprocals and the quotients
+    cover many binades, and some quotients fall within a few fp32 ulps of an
+    E4M3 rounding boundary): codes and scales bit-exact."""
+    M, K = 2048, 8704
+    rng = np.random.default_rng(123)
+    x = rng.standard_normal((M, K), dtype=np.float32)
+    x *= (2.0 ** rng.uniform(-30, 30, size=(M, K // 128))).astype(np.float32).repeat(128, axis=1)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    q, sa = fp8act.fp8_act_quant(xb.cuda())
+    torch.cuda.synchronize()
+    q_ref, sa_ref = oracle.act_quant(inputs.bf16_bits(xb))
+    assert np.array_equal(sa.cpu().numpy(), sa_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
