@@ -28,7 +28,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// 16-byte load of data read exactly once: read-only path, no L1 allocation.
+// 16-byte load of data read exactly once and never written while any kernel
+// of the library runs (the weights): read-only path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 v;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -40,13 +41,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
 // 32-byte aligned): bytes 0..15 to lo, 16..31 to hi.
 __device__ __forceinline__ void ld_stream_v8(const void* p, uint4& lo, uint4& hi) {
     asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-        : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
-        : "l"(p));
-}
-
-// 32-byte load of data that many CTAs re-read (kept in L1); `p` 32-byte aligned.
-__device__ __forceinline__ void ld_ro_v8(const void* p, uint4& lo, uint4& hi) {
-    asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
         : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
         : "l"(p));
 }
@@ -63,9 +57,45 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// 16-byte load of data that many CTAs re-read (kept in L1).
-__device__ __forceinline__ uint4 ld_shared_ro_v4(const void* p) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
+// Loads of data that the previous grid in the stream may write: activation
+// codes, activation scales and bf16 inputs. A kernel launched with
+// programmatic dependent launch starts while that grid may still run, and
+// reads such data only after griddepcontrol.wait. These loads are volatile
+// and clobber memory, so the compiler keeps them after the wait (a plain asm
+// load, which it sees as a pure function of the address, or __ldg may be
+// hoisted above it), and they take the coherent path (ld.global.nc assumes
+// the data cannot change while the kernel runs). The weight loads above stay
+// free to move: the weights never change.
+
+// 16 bytes, kept in L1 (re-read by many warps).
+__device__ __forceinline__ uint4 ld_dep_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+    return v;
+}
+
+// 16 bytes read once (no L1 allocation).
+__device__ __forceinline__ uint4 ld_dep_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+    return v;
+}
+
+// 32 bytes in one access (`p` 32-byte aligned), kept in L1: bytes 0..15 to lo, 16..31 to hi.
+__device__ __forceinline__ void ld_dep_v8(const void* p, uint4& lo, uint4& hi) {
+    asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+                 : "l"(p)
+                 : "memory");
+}
+
+// One fp32 value.
+__device__ __forceinline__ float ld_dep_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
 }
 
 }  // namespace fp8act

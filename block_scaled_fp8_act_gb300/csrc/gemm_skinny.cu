@@ -202,7 +202,7 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
             const bool ok = gi < groups;
             const int r = ok ? gi / KB : 0;
             const int kb = ok ? gi % KB : 0;
-            const uint4 v = ok ? ld_stream_v4(q + (static_cast<int64_t>(m0 + r) * K + kb * kGroup + 8 * hl) * 2)
+            const uint4 v = ok ? ld_dep_stream_v4(q + (static_cast<int64_t>(m0 + r) * K + kb * kGroup + 8 * hl) * 2)
                                : zero;
             uint2 codes;
             const float sg = quant_group_halfwarp(v, codes);
@@ -257,10 +257,10 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                     const int m = m0 + 8 * j + g;
                     const bool ok_x = m < M;
                     const uint8_t* x_r = q + (static_cast<int64_t>(m) * K + 16 * t) * 2 + off;
-                    const uint4 x0 = ok_x ? ld_shared_ro_v4(x_r) : zero;
-                    const uint4 x1 = ok_x ? ld_shared_ro_v4(x_r + 16) : zero;
-                    const uint4 x2 = ok_x ? ld_shared_ro_v4(x_r + 128) : zero;
-                    const uint4 x3 = ok_x ? ld_shared_ro_v4(x_r + 144) : zero;
+                    const uint4 x0 = ok_x ? ld_dep_v4(x_r) : zero;
+                    const uint4 x1 = ok_x ? ld_dep_v4(x_r + 16) : zero;
+                    const uint4 x2 = ok_x ? ld_dep_v4(x_r + 128) : zero;
+                    const uint4 x3 = ok_x ? ld_dep_v4(x_r + 144) : zero;
                     const uint32_t xw[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
                                              x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
                     float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -297,10 +297,10 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                         xhi[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + off + kHiOff) : zero;
                     } else if constexpr (kWide) {
                         xlo[u] = xhi[u] = zero;
-                        if (ok_k && ok_x) ld_ro_v8(x_r + off, xlo[u], xhi[u]);
+                        if (ok_k && ok_x) ld_dep_v8(x_r + off, xlo[u], xhi[u]);
                     } else {
-                        xlo[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off) : zero;
-                        xhi[u] = (ok_k && ok_x) ? ld_shared_ro_v4(x_r + off + 64) : zero;
+                        xlo[u] = (ok_k && ok_x) ? ld_dep_v4(x_r + off) : zero;
+                        xhi[u] = (ok_k && ok_x) ? ld_dep_v4(x_r + off + 64) : zero;
                     }
                 }
 #pragma unroll
@@ -318,8 +318,8 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                             if (c0 < M) sa0 = sa_s[(c0 - m0) * KB + kb];
                             if (c0 + 1 < M) sa1 = sa_s[(c0 + 1 - m0) * KB + kb];
                         } else {
-                            if (c0 < M) sa0 = __ldg(sa + static_cast<int64_t>(c0) * KB + kb);
-                            if (c0 + 1 < M) sa1 = __ldg(sa + static_cast<int64_t>(c0 + 1) * KB + kb);
+                            if (c0 < M) sa0 = ld_dep_f32(sa + static_cast<int64_t>(c0) * KB + kb);
+                            if (c0 + 1 < M) sa1 = ld_dep_f32(sa + static_cast<int64_t>(c0 + 1) * KB + kb);
                         }
                         const float s0 = sa0 * s_w;
                         const float s1 = sa1 * s_w;

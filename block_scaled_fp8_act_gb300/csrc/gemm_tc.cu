@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
             for (int k = 0; k < nk; ++k, ++i) {
                 const int b = i & 1;
                 const int kb = kb_begin + k;
-                const float scale = row_ok ? __ldg(sa_row + kb) * __ldg(sw_row + kb) : 0.f;
+                const float scale = row_ok ? ld_dep_f32(sa_row + kb) * __ldg(sw_row + kb) : 0.f;
                 if (!failed && !ptx::mbar_wait(tfull0 + 8 * b, (i >> 1) & 1)) flag_error(failed, 8u);
                 tc::fence_after_sync();
                 if constexpr (C::kCols == 64) {

@@ -85,7 +85,7 @@ __device__ __forceinline__ void act_quant_body(const Map& map, int64_t groups) {
             qg[u] = nullptr;
             sg[u] = nullptr;
             if (g < groups) map.at(g, xg, qg[u], sg[u]);
-            v[u] = g < groups ? ld_stream_v4(xg + hl) : make_uint4(0, 0, 0, 0);
+            v[u] = g < groups ? ld_dep_stream_v4(xg + hl) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kActUnroll; ++u) {

@@ -368,8 +368,9 @@ def test_new_paths_capture_in_cuda_graph_and_match_eager(fp8act):
             fp8act.fp8_block_gemm_grouped([(q, sa, p.w, p.sw) for (q, sa), p in zip(qsa2, ps)], outs=og, stream=s)
     g.replay()
     torch.cuda.synchronize()
-    for a, b in zip(eager16 + eagerf + eagerg, o16 + of + og):
-        assert torch.equal(a, b)
+    names = [f"{call} {si}" for call in ("w8a16", "fused", "grouped") for si in range(len(ps))]
+    for name, a, b in zip(names, eager16 + eagerf + eagerg, o16 + of + og):
+        assert torch.equal(a, b), (name, (a.float() - b.float()).abs().max().item())
 
 
 def test_new_paths_write_nothing_outside_out(fp8act):
@@ -402,6 +403,96 @@ def test_fused_at_its_shared_memory_limit(fp8act):
     sw = torch.ones((2, (24576 + 1024) // 128), dtype=torch.float32, device="cuda")
     with pytest.raises(fp8act.Fp8ActError):
         fp8act.fp8_linear(x, w, sw)
+
+
+# ------------------------------------------- more shapes and call patterns
+EXTRA_SHAPES = [(3, 1000, 10240), (1, 17, 65536), (8, 2056, 5120), (5, 130, 30720)]
+
+
+@pytest.mark.parametrize("M,N,K", EXTRA_SHAPES)
+def test_gemm_long_k_and_ragged_n(fp8act, M, N, K):
+    """Few 16-row tiles against long K (N = 17, K = 65536: two tiles of 512
+    K blocks each), N not a multiple of 16 or 128; the W8A16 and fused calls
+    on the same shapes, and the fused result equal bit for bit to the
+    two-launch one."""
+    from parity_util import Problem
+    p = Problem(N, K, seed=N + K)
+    p.run_and_compare(M, seed=M + 3)
+    _w8a16_compare(fp8act, p, M, seed=M + 4)
+    xd, out32 = _linear_compare(fp8act, p, M, seed=M + 5)
+    q, sa = fp8act.fp8_act_quant(xd)
+    ref32 = fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw)
+    torch.cuda.synchronize()
+    assert torch.equal(out32, ref32)
+
+
+def test_gemm_repeated_and_interleaved_calls(fp8act):
+    """The five shapes called in turn, three times over in alternating order
+    on one stream (back-to-back launches that overlap through programmatic
+    dependent launch), give the same bits every time."""
+    ps = [problem(si) for si in range(len(SHAPES))]
+    acts = [p.activations(1 + 2 * si, seed=70 + si)[:2] for si, p in enumerate(ps)]
+    first = [fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw) for (q, sa), p in zip(acts, ps)]
+    later = []
+    for r in range(3):
+        order = list(range(len(ps)))[::(-1 if r % 2 else 1)]
+        res = {i: fp8act.fp8_block_gemm_f32(acts[i][0], acts[i][1], ps[i].w, ps[i].sw) for i in order}
+        later.append([res[i] for i in range(len(ps))])
+    torch.cuda.synchronize()
+    for res in later:
+        for a, b in zip(first, res):
+            assert torch.equal(a, b)
+
+
+def test_gemm_concurrent_streams(fp8act):
+    """Two streams issuing GEMMs at the same time: every result equals the
+    serial one."""
+    p0, p2 = problem(0), problem(2)
+    q0, sa0 = p0.activations(2, seed=81)[:2]
+    q2, sa2 = p2.activations(6, seed=82)[:2]
+    r0 = fp8act.fp8_block_gemm_f32(q0, sa0, p0.w, p0.sw)
+    r2 = fp8act.fp8_block_gemm_f32(q2, sa2, p2.w, p2.sw)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    o0 = [torch.empty_like(r0) for _ in range(16)]
+    o2 = [torch.empty_like(r2) for _ in range(16)]
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    for a, b in zip(o0, o2):
+        fp8act.fp8_block_gemm_f32(q0, sa0, p0.w, p0.sw, a, stream=s1)
+        fp8act.fp8_block_gemm_f32(q2, sa2, p2.w, p2.sw, b, stream=s2)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, r0) for a in o0) and all(torch.equal(b, r2) for b in o2)
+
+
+def test_first_calls_on_a_stream_inside_capture(fp8act):
+    """A stream whose first GEMM and fused calls are inside a graph capture:
+    replays match the eager results, and so do eager calls on that stream
+    afterwards."""
+    p = problem(2)
+    q, sa = p.activations(4, seed=91)[:2]
+    x = inputs.activations_bf16(4, p.K, seed=92).cuda()
+    ref = fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw)
+    ref_f = fp8act.fp8_linear_f32(x, p.w, p.sw)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    out = torch.empty_like(ref)
+    out_f = torch.empty_like(ref_f)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw, out, stream=s)
+            fp8act.fp8_linear_f32(x, p.w, p.sw, out_f, stream=s)
+    for _ in range(3):
+        out.zero_()
+        out_f.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref) and torch.equal(out_f, ref_f)
+    with torch.cuda.stream(s):
+        e = fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw, stream=s)
+    torch.cuda.synchronize()
+    assert torch.equal(e, ref)
 
 
 @pytest.mark.parametrize("si", [1, 0])
