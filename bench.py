@@ -537,6 +537,8 @@ def main() -> None:
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode",
                     help="decode (M=1, the headline), verify, batched or prefill")
     ap.add_argument("--m", type=int, default=None, help="token count for the chosen workload")
+    ap.add_argument("--steps-per-graph", type=int, default=10,
+                    help="consecutive steps captured in one CUDA graph (timed steps stay exactly --steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -571,12 +573,29 @@ def main() -> None:
     else:
         weights = Weights(device)
     wl = Workload(M, weights, device, weight_only=weight_only, grouped=grouped, fused=fused)
+    # One graph per step, and graphs of S consecutive steps (step i uses weight copy i mod
+    # copies, as in the one-step graphs), the way a serving loop captures a whole forward
+    # pass of many layers: programmatic dependent launch overlaps consecutive kernels
+    # inside a graph but not across graph launches.
+    S = max(1, min(args.steps_per_graph, args.steps))
     graphs = [capture(lambda c=c: wl.enqueue_step(c, stream), stream) for c in range(wl.copies)]
+    multi = [capture(lambda j=j: [wl.enqueue_step((j * S + s) % wl.copies, stream) for s in range(S)], stream)
+             for j in range(wl.copies)] if S > 1 else graphs
     launches_per_step = wl.launches_per_step()
 
+    def replay_steps(n: int) -> None:
+        """Exactly n steps: n // S replays of the S-step graphs, then single steps."""
+        for j in range(n // S):
+            multi[j % len(multi)].replay()
+        for i in range(n // S * S, n):
+            graphs[i % len(graphs)].replay()
+
     # ---- timed region: K steps of the whole path, graphs replayed back to back
-    for i in range(args.warmup):
-        graphs[i % len(graphs)].replay()
+    with torch.cuda.stream(stream):
+        replay_steps(args.warmup)
+        if S > 1:
+            for g in multi:  # first replays (graph upload) stay out of the timed region
+                g.replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -584,8 +603,7 @@ def main() -> None:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             start.record(stream)
-            for i in range(args.steps):
-                graphs[i % len(graphs)].replay()
+            replay_steps(args.steps)
             end.record(stream)
         end.synchronize()
         torch.cuda.synchronize()
@@ -669,7 +687,7 @@ def main() -> None:
                       "us_p90": round(hi * 1e6, 3), "gbs": round(algorithmic_quant_bytes(M, K) / med / 1e9, 1),
                       "frac": round(algorithmic_quant_bytes(M, K) / med / 1e9 / float(peaks["hbm_gbs"]), 4)}
                      for (_, K), (med, lo, hi) in zip(wl.shapes, quant_kernel_times(wl, stream))]
-    del graphs
+    del graphs, multi
     torch.cuda.synchronize()
     result = {
         "metric": METRIC if args.workload == "decode" else f"block-FP8 linear, {desc}",
@@ -681,7 +699,8 @@ def main() -> None:
         "config": {"workload": desc, "M": M, "shapes": [list(s) for s in wl.shapes],
                    "l2": f"inputs larger than L2: {wl.copies} rotating weight copies "
                          f"({wl.copies * sum(N * K for N, K in wl.shapes) / 1e6:.0f} MB), no flush",
-                   "graphs": f"each step is one CUDA graph replay ({launches_per_step} kernels)",
+                   "graphs": f"{S} steps per CUDA graph replay ({launches_per_step} kernels per step)",
+                   "steps_per_graph": S,
                    "parallelism": f"replicas x{world}"},
         "us_per_call": per_shape,
         "act_quant": act_quant,
