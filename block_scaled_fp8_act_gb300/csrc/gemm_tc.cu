@@ -99,6 +99,15 @@ __device__ __forceinline__ void flag_error(bool& failed, unsigned int code) {
     }
 }
 
+// d0 += a0 * s and d1 += a1 * s as one packed two-lane fp32 FMA: two
+// independent IEEE round-to-nearest FMAs, the same bits as two fmaf calls in
+// half the instructions.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float s) {
+    const float2 r = __ffma2_rn(make_float2(a0, a1), make_float2(s, s), make_float2(d0, d1));
+    d0 = r.x;
+    d1 = r.y;
+}
+
 template <bool kF32Out>
 __device__ __forceinline__ void store_one(void* out, int64_t idx, float v) {
     if constexpr (kF32Out)
@@ -257,15 +266,16 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                 if (!failed && !ptx::mbar_wait(tfull0 + 8 * b, (i >> 1) & 1)) flag_error(failed, 8u);
                 tc::fence_after_sync();
                 if constexpr (C::kCols == 64) {
-                    // both 32-column halves in flight, one wait
+                    // both 32-column halves in flight, one wait; packed FMAs (7% off the
+                    // batched-decode GEMM; at BN = 256 they cost spills and lost 7.5%)
                     uint32_t r0[32], r1[32];
                     tc::ld_32x32b_x32(t_row + b * BN, r0);
                     tc::ld_32x32b_x32(t_row + b * BN + 32, r1);
                     tc::wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        acc[j] = fmaf(__uint_as_float(r0[j]), scale, acc[j]);
-                        acc[32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[32 + j]);
+                    for (int j = 0; j < 32; j += 2) {
+                        fma2(acc[j], acc[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), scale);
+                        fma2(acc[32 + j], acc[33 + j], __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]), scale);
                     }
                 } else {
                     // two rounds of 64 columns, both 32-column loads of a round in flight
