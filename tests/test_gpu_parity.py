@@ -103,6 +103,16 @@ def test_gemm_prefill_sampled_rows(fp8act, si):
     problem(si).run_and_compare(4096, inputs.activation_seed(si, 10), rows=rows)
 
 
+@pytest.mark.parametrize("N,K", [(2600, 1024), (5000, 512)])
+def test_gemm_prefill_ragged_n(fp8act, N, K):
+    """M = 4096 with N past the last full 256-wide tile: the last tile's rows
+    beyond N read as zero, its scale blocks end inside the tile, and nothing
+    is stored past N."""
+    from parity_util import Problem, sample_rows
+    rows = sample_rows(4096, 24, seed=N)
+    Problem(N, K, seed=N + K).run_and_compare(4096, seed=7, rows=rows)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 17, 128), (3, 200, 256), (8, 1000, 384), (9, 130, 512),
                                    (16, 4096, 1024), (63, 300, 640), (65, 257, 768),
                                    (127, 129, 256), (129, 520, 1152), (300, 384, 384)])
