@@ -65,13 +65,15 @@ struct TcCfg {
     // Warp roles: warp 0 TMA producer, warp 1 MMA issuer, then the eight
     // epilogue warps. The 256-wide tile runs 12 warps (three warpgroups) so
     // that warpgroup 0 (producer, MMA, two idle warps) can hand registers to
-    // the two epilogue warpgroups with setmaxnreg: 128 x 56 + 256 x 224 =
-    // 64512 = 384 x 168, exactly the launch's registers.
+    // the two epilogue warpgroups with setmaxnreg: 128 x 24 + 256 x 240 =
+    // 64512 = 384 x 168, exactly the launch's registers. The producer and MMA
+    // loops fit in 24 registers; the epilogue's 128 accumulators, 64 staged
+    // TMEM values and packed FMAs need the 240 (no spills).
     static constexpr int kCtrlWarps = BN == 256 ? 4 : 2;
     static constexpr int kThreads = (kCtrlWarps + kEpiWarps) * 32;
     static constexpr int kRegsLaunch = 168;  // per thread at launch (ptxas, __launch_bounds__)
-    static constexpr int kRegsCtrl = 56;
-    static constexpr int kRegsEpi = 224;
+    static constexpr int kRegsCtrl = 24;
+    static constexpr int kRegsEpi = 240;
     static_assert(BN != 256 || 128 * kRegsCtrl + 256 * kRegsEpi <= kThreads * kRegsLaunch,
                   "register split exceeds the launch's registers");
     static constexpr int kBBytes = BN * kGroup;
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                 tc::fence_after_sync();
                 if constexpr (C::kCols == 64) {
                     // both 32-column halves in flight, one wait; packed FMAs (7% off the
-                    // batched-decode GEMM; at BN = 256 they cost spills and lost 7.5%)
+                    // batched-decode GEMM)
                     uint32_t r0[32], r1[32];
                     tc::ld_32x32b_x32(t_row + b * BN, r0);
                     tc::ld_32x32b_x32(t_row + b * BN + 32, r1);
@@ -278,7 +280,10 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                         fma2(acc[32 + j], acc[33 + j], __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]), scale);
                     }
                 } else {
-                    // two rounds of 64 columns, both 32-column loads of a round in flight
+                    // two rounds of 64 columns, both 32-column loads of a round in flight;
+                    // packed FMAs (13% off the prefill GEMM; they need the 240-register
+                    // epilogue, at 224 ptxas spilled and they lost 7.5%)
+                    const float2 s2 = make_float2(scale, scale);
 #pragma unroll
                     for (int c = 0; c < C::kCols / 64; ++c) {
                         uint32_t r0[32], r1[32];
@@ -286,9 +291,18 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                         tc::ld_32x32b_x32(t_row + b * BN + c * 64 + 32, r1);
                         tc::wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            acc[c * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[c * 64 + j]);
-                            acc[c * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[c * 64 + 32 + j]);
+                        for (int j = 0; j < 32; j += 2) {
+                            float2 x = __ffma2_rn(make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])), s2,
+                                                  make_float2(acc[c * 64 + j], acc[c * 64 + j + 1]));
+                            acc[c * 64 + j] = x.x;
+                            acc[c * 64 + j + 1] = x.y;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            float2 x = __ffma2_rn(make_float2(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])), s2,
+                                                  make_float2(acc[c * 64 + 32 + j], acc[c * 64 + 33 + j]));
+                            acc[c * 64 + 32 + j] = x.x;
+                            acc[c * 64 + 33 + j] = x.y;
                         }
                     }
                 }
