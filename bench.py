@@ -317,6 +317,18 @@ def capture(fn, stream) -> torch.cuda.CUDAGraph:
     return g
 
 
+def graph_schedule(n: int, steps_per_graph: int, copies: int) -> list[tuple[str, int]]:
+    """Replays that run exactly n steps: ("multi", j) replays S-step graph j (its
+    steps use weight copies (j S + s) mod copies), then ("single", c) replays
+    the one-step graph of copy c for the remainder. Step i always uses weight
+    copy i mod copies."""
+    S = steps_per_graph
+    out = [("multi", j % copies) for j in range(n // S)] if S > 1 else []
+    done = n // S * S if S > 1 else 0
+    out += [("single", i % copies) for i in range(done, n)]
+    return out
+
+
 def time_graphs(graphs, steps: int, warmup: int, stream) -> float:
     """Seconds per replay, replaying graphs round-robin, CUDA events on `stream`."""
     for i in range(warmup):
@@ -585,10 +597,8 @@ def main() -> None:
 
     def replay_steps(n: int) -> None:
         """Exactly n steps: n // S replays of the S-step graphs, then single steps."""
-        for j in range(n // S):
-            multi[j % len(multi)].replay()
-        for i in range(n // S * S, n):
-            graphs[i % len(graphs)].replay()
+        for kind, c in graph_schedule(n, S, wl.copies):
+            (multi if kind == "multi" else graphs)[c].replay()
 
     # ---- timed region: K steps of the whole path, graphs replayed back to back
     with torch.cuda.stream(stream):
