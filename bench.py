@@ -80,7 +80,7 @@ FUSED = {"decode-fused"}
 
 
 def gemm_kernel_name(M: int) -> str:
-    return "gemm_skinny_kernel" if M <= 16 else "gemm_tc_kernel"
+    return "gemm_skinny_kernel" if M <= 16 else ("gemm_midm_kernel" if M <= 48 else "gemm_tc_kernel")
 WEIGHT_COPIES = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
@@ -119,6 +119,7 @@ KERNEL_SOURCES = {
     "gemm_skinny_kernel": ("gemm_skinny.cu", "common.cuh", "sm100_ptx.cuh"),
     "gemm_skinny_grouped_kernel": ("gemm_skinny.cu", "common.cuh", "sm100_ptx.cuh"),
     "gemm_tc_kernel": ("gemm_tc.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
+    "gemm_midm_kernel": ("gemm_midm.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
 }
 
 

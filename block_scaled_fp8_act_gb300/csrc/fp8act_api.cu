@@ -11,7 +11,12 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kGroup = 128;
-constexpr int kSkinnyMaxM = 16;  // M up to this streams weights through mma.sync; above, tcgen05 tiles
+constexpr int kSkinnyMaxM = 16;  // M up to this streams weights through mma.sync; above, tcgen05 kernels
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // the tcgen05 kernels' default wait bound (2 s)
+
+// Failure-path test hook (fp8act_set_wait_limit): < 0 = the default bound.
+std::atomic<long long> g_wait_limit_ns{-1};
+std::atomic<int> g_withhold_first_load{0};
 
 // Per-device facts looked up once: -1 = unknown, 0 = unsupported, else SM count.
 std::atomic<int> g_device_sms[kMaxDevices];
@@ -49,6 +54,21 @@ int launch_status(cudaError_t e) {
 // K: positive multiple of 128; rows*K must fit in int64 and each of M, N, K in int.
 int check_k(int K) { return (K <= 0 || K % kGroup) ? FP8ACT_ERR_SHAPE : FP8ACT_OK; }
 
+// The GEMM kernel for M tokens: weight streaming through mma.sync up to 16,
+// the swap-AB tcgen05 weight-streaming kernel up to 128, token-tiled tcgen05
+// tiles above (prefill).
+cudaError_t launch_gemm_any(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N,
+                            int K, void* out, bool out_f32, int sms, cudaStream_t s) {
+    if (M <= kSkinnyMaxM) return fp8act::launch_gemm_skinny(q, sa, w, sw, M, N, K, out, out_f32, sms, s);
+    if (M <= fp8act::kMidMaxM) {
+        // cudaErrorNotSupported: the CTA's scale table would not fit (very long K
+        // on few tiles); the token-tiled kernel below handles any shape.
+        const cudaError_t e = fp8act::launch_gemm_midm(q, sa, w, sw, M, N, K, out, out_f32, sms, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    return fp8act::launch_gemm_tc(q, sa, w, sw, M, N, K, out, out_f32, sms, s);
+}
+
 int gemm_common(const void* q, const float* sa, const void* w, const float* sw, int M, int N, int K, void* out,
                 bool out_f32, void* stream) {
     if (M < 0 || N < 0) return FP8ACT_ERR_SHAPE;
@@ -63,9 +83,7 @@ int gemm_common(const void* q, const float* sa, const void* w, const float* sw, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint8_t* q8 = static_cast<const uint8_t*>(q);
     const uint8_t* w8 = static_cast<const uint8_t*>(w);
-    if (M <= kSkinnyMaxM)
-        return launch_status(fp8act::launch_gemm_skinny(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
-    return launch_status(fp8act::launch_gemm_tc(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
+    return launch_status(launch_gemm_any(q8, sa, w8, sw, M, N, K, out, out_f32, sms, s));
 }
 
 constexpr int kMaxGrouped = 16;
@@ -108,9 +126,9 @@ int gemm_grouped_common(const fp8act_gemm_problem* problems, int count, bool out
     for (int i = 0; i < count; ++i) {
         const fp8act_gemm_problem& p = problems[i];
         if (p.M <= kSkinnyMaxM || p.N == 0) continue;
-        if (int e = launch_status(fp8act::launch_gemm_tc(static_cast<const uint8_t*>(p.q_e4m3), p.sa,
-                                                         static_cast<const uint8_t*>(p.w_e4m3), p.sw, p.M, p.N, p.K,
-                                                         p.out, out_f32, sms, s)))
+        if (int e = launch_status(launch_gemm_any(static_cast<const uint8_t*>(p.q_e4m3), p.sa,
+                                                  static_cast<const uint8_t*>(p.w_e4m3), p.sw, p.M, p.N, p.K, p.out,
+                                                  out_f32, sms, s)))
             return e;
     }
     return FP8ACT_OK;
@@ -146,6 +164,14 @@ int w8a16_common(const void* x, const void* w, const float* sw, int M, int N, in
 }
 
 }  // namespace
+
+namespace fp8act {
+unsigned long long tile_wait_limit_ns() {
+    const long long v = g_wait_limit_ns.load(std::memory_order_relaxed);
+    return v < 0 ? kDefaultWaitNs : static_cast<unsigned long long>(v);
+}
+bool tile_withhold_first_load() { return g_withhold_first_load.load(std::memory_order_relaxed) != 0; }
+}  // namespace fp8act
 
 extern "C" {
 
@@ -254,10 +280,17 @@ int fp8act_check_status(void* stream) {
         cudaGetLastError();
         return FP8ACT_ERR_CUDA;
     }
-    if (fp8act::read_and_clear_tc_error()) return FP8ACT_ERR_TIMEOUT;
+    const unsigned int tc = fp8act::read_and_clear_tc_error();
+    const unsigned int mid = fp8act::read_and_clear_midm_error();
+    return (tc | mid) ? FP8ACT_ERR_TIMEOUT : FP8ACT_OK;
+}
+
+int fp8act_set_wait_limit(long long limit_ns, int withhold_first_load) {
+    g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    g_withhold_first_load.store(withhold_first_load ? 1 : 0, std::memory_order_relaxed);
     return FP8ACT_OK;
 }
 
-int fp8act_version(void) { return 100; }
+int fp8act_version(void) { return 200; }
 
 }  // extern "C"

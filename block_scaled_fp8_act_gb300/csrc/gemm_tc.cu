@@ -39,9 +39,12 @@
 // partials through distributed shared memory, in rank order (deterministic),
 // and stores them. No global scratch, no atomics.
 //
-// Every mbarrier wait is bounded; a timeout sets the error word read by
-// fp8act_check_status() and the kernel runs to completion on whatever data it
-// has (never a hang). TMEM is always freed.
+// Failure handling: every wait is bounded (the bound is a launch argument).
+// The first wait that gives up sets the device error word read by
+// fp8act_check_status() and a CTA-wide abort flag; every role then stops
+// issuing work, the producer waits (bounded) for the copies it already
+// issued, the MMA thread for the MMAs it already issued, and only then is
+// TMEM freed and the CTA leaves (never a hang, no copy or MMA in flight at exit).
 #include <atomic>
 
 #include "common.cuh"
@@ -83,7 +86,8 @@ struct TcCfg {
     static constexpr int kCols = BN / 2;                   // output columns per epilogue thread
     static constexpr int kRedStride = BN + 4;  // row stride (floats) of the parked partial tile: 16-byte
                                                // aligned rows, rows 4 banks apart (conflict-free v4)
-    static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
+    static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;  // + barriers, TMEM slot, abort flag
+    static_assert(16 * kStages + 32 + 8 + 8 + 4 <= 256, "barrier area");
     static_assert(BM * kRedStride * 4 <= kStages * kStageBytes, "partial tile must fit in the stages");
 };
 
@@ -92,13 +96,13 @@ struct TcArgs {
     const float* sw;
     void* out;
     int M, N, K, KB, NB;
+    unsigned long long wait_ns;  // bound of every wait that can give up (test hook shortens it)
+    int withhold;                // test hook: the producer never issues the CTA's first K group
 };
 
-__device__ __forceinline__ void flag_error(bool& failed, unsigned int code) {
-    if (!failed) {
-        failed = true;
-        atomicOr(&g_tc_error, code);
-    }
+__device__ __forceinline__ void fail(volatile int* abort, unsigned int code) {
+    *abort = 1;
+    atomicOr(&g_tc_error, code);
 }
 
 // d0 += a0 * s and d1 += a1 * s as one packed two-lane fp32 FMA: two
@@ -133,8 +137,10 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
     const uint32_t empty0 = full0 + 8 * C::kStages;    // [kStages] MMAs done reading
     const uint32_t tfull0 = empty0 + 8 * C::kStages;   // [2] accumulator ready
     const uint32_t tempty0 = tfull0 + 16;              // [2] accumulator drained
-    const uint32_t tmem_slot = tempty0 + 16;
+    const uint32_t drain = tempty0 + 16;               // MMA thread: every issued MMA has completed
+    const uint32_t tmem_slot = drain + 8;
     volatile uint32_t* const tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+    volatile int* const abort = reinterpret_cast<volatile int*>(base_ptr + (tmem_slot - base) + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -158,6 +164,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
             ptx::mbar_init(tfull0 + 8 * b, 1);
             ptx::mbar_init(tempty0 + 8 * b, kEpiWarps);
         }
+        ptx::mbar_init(drain, 1);
+        *abort = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
             ptx::prefetch_tensormap(&tmap_a);
             ptx::prefetch_tensormap(&tmap_b);
             const uint64_t policy = ptx::policy_evict_last();  // both operands are re-read by other tiles
-            bool failed = false;
+            const bool skip0 = a.withhold != 0;
             // stage use i -> tile blockIdx.x + (i / nk) * gridDim.x, K group kb_begin + i % nk
             auto tile_mn = [&](int i, int& m0_, int& n0_) {
                 const int tile = blockIdx.x + (i / nk) * gridDim.x;
@@ -195,7 +203,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                 n0_ = (tile / mtiles) * BN;
             };
             const int pre = total < C::kStages ? total : C::kStages;
-            for (int i = 0; i < pre; ++i) {  // weights: independent of the previous grid
+            for (int i = skip0 ? 1 : 0; i < pre; ++i) {  // weights: independent of the previous grid
                 int m0_, n0_;
                 tile_mn(i, m0_, n0_);
                 ptx::mbar_arrive_expect_tx(full0 + 8 * i, C::kStageBytes);
@@ -203,34 +211,49 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                                  (kb_begin + i % nk) * kGroup, n0_, policy);
             }
             ptx::griddep_wait();  // activations are the previous grid's output
-            for (int i = 0; i < pre; ++i) {
+            for (int i = skip0 ? 1 : 0; i < pre; ++i) {
                 int m0_, n0_;
                 tile_mn(i, m0_, n0_);
                 ptx::tma_load_2d(base + i * C::kStageBytes, &tmap_a, full0 + 8 * i, (kb_begin + i % nk) * kGroup, m0_,
                                  policy);
             }
+            int issued = pre;
             for (int i = pre; i < total; ++i) {
                 const int s = i % C::kStages;
                 int m0_, n0_;
                 tile_mn(i, m0_, n0_);
-                if (!failed && !ptx::mbar_wait(empty0 + 8 * s, ((i / C::kStages) - 1) & 1)) flag_error(failed, 1u);
+                if (!ptx::mbar_wait_or_abort(empty0 + 8 * s, ((i / C::kStages) - 1) & 1, a.wait_ns, abort)) {
+                    fail(abort, 1u);
+                    break;
+                }
                 ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
                 ptx::tma_load_2d(base + s * C::kStageBytes + kABytes, &tmap_b, full0 + 8 * s,
                                  (kb_begin + i % nk) * kGroup, n0_, policy);
                 ptx::tma_load_2d(base + s * C::kStageBytes, &tmap_a, full0 + 8 * s, (kb_begin + i % nk) * kGroup, m0_,
                                  policy);
+                issued = i + 1;
             }
+            // Every copy issued must land before the CTA may leave: wait for
+            // the last use of each stage (the MMA thread has usually seen it).
+            for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+                if (!(skip0 && i == 0) && !ptx::mbar_wait(full0 + 8 * (i % C::kStages), (i / C::kStages) & 1))
+                    fail(abort, 16u);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_e4m3_f32(BM, BN);
-            bool failed = false;
             for (int i = 0; i < total; ++i) {
                 const int s = i % C::kStages;
                 const int b = i & 1;
-                if (!failed && !ptx::mbar_wait(full0 + 8 * s, (i / C::kStages) & 1)) flag_error(failed, 2u);
-                if (i >= 2 && !failed && !ptx::mbar_wait(tempty0 + 8 * b, ((i >> 1) - 1) & 1)) flag_error(failed, 4u);
+                if (!ptx::mbar_wait_or_abort(full0 + 8 * s, (i / C::kStages) & 1, a.wait_ns, abort)) {
+                    fail(abort, 2u);
+                    break;
+                }
+                if (i >= 2 && !ptx::mbar_wait_or_abort(tempty0 + 8 * b, ((i >> 1) - 1) & 1, a.wait_ns, abort)) {
+                    fail(abort, 4u);
+                    break;
+                }
                 tc::fence_after_sync();
                 const uint32_t a_tile = base + s * C::kStageBytes;
                 const uint32_t b_tile = a_tile + kABytes;
@@ -241,6 +264,9 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                 tc::commit(empty0 + 8 * s);   // the stage's smem may be refilled once these MMAs finish
                 tc::commit(tfull0 + 8 * b);   // the accumulator holds this K group's product
             }
+            // No MMA may still run when TMEM is freed or the CTA leaves.
+            tc::commit(drain);
+            if (!ptx::mbar_wait(drain, 0)) fail(abort, 32u);
         }
     }
     } else {
@@ -250,7 +276,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + hf * C::kCols;
         bool failed = false;
         int i = 0;  // accumulator uses so far
-        for (int t = 0; t < my_tiles; ++t) {
+        for (int t = 0; t < my_tiles && !failed; ++t) {
             const int tile = blockIdx.x + t * gridDim.x;
             m0 = (tile % mtiles) * BM;
             n0 = (tile / mtiles) * BN;
@@ -265,7 +291,12 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                 const int b = i & 1;
                 const int kb = kb_begin + k;
                 const float scale = row_ok ? ld_dep_f32(sa_row + kb) * __ldg(sw_row + kb) : 0.f;
-                if (!failed && !ptx::mbar_wait(tfull0 + 8 * b, (i >> 1) & 1)) flag_error(failed, 8u);
+                // the whole warp decides together (tcgen05.ld is warp-collective)
+                if (!__all_sync(0xffffffffu, ptx::mbar_wait_or_abort(tfull0 + 8 * b, (i >> 1) & 1, a.wait_ns, abort))) {
+                    if (lane == 0) fail(abort, 8u);
+                    failed = true;
+                    break;
+                }
                 tc::fence_after_sync();
                 if constexpr (C::kCols == 64) {
                     // both 32-column halves in flight, one wait; packed FMAs (7% off the
@@ -310,7 +341,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(tempty0 + 8 * b);
             }
-            if (splits == 1 && m < a.M) {
+            if (splits == 1 && m < a.M && !failed) {
                 // store this thread's row segment directly
                 const int nstart = n0 + hf * C::kCols;
                 if constexpr (kF32Out) {
@@ -349,10 +380,12 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
 
     if constexpr (BN == 128) {  // split K is only chosen with 128-wide tiles
     if (splits > 1) {
-        // Park the partial tile in the idle stage memory (every MMA has
-        // completed and every TMA copy has landed: the epilogue saw the last
-        // accumulator), then reduce a slice of rows across the cluster.
+        // Park the partial tile in the idle stage memory once every role has
+        // left its loop (every issued copy has landed, every issued MMA has
+        // completed), then reduce a slice of rows across the cluster.
+        __syncthreads();
         float* red = reinterpret_cast<float*>(base_ptr);
+        const bool ok = *abort == 0;
         if (epi) {
 #pragma unroll
             for (int j = 0; j < C::kCols; j += 4)
@@ -386,7 +419,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                         v.w += part[c].w;
                     }
                 const int m = m0 + r, n = n0 + col;
-                if (m < a.M) {
+                if (ok && m < a.M) {
                     const int64_t o = static_cast<int64_t>(m) * a.N + n;
                     if (n + 3 < a.N && (a.N & 3) == 0) {
                         if constexpr (kF32Out) {
@@ -519,6 +552,8 @@ cudaError_t launch_gemm_tc(const uint8_t* q, const float* sa, const uint8_t* w, 
     a.K = K;
     a.KB = K / kGroup;
     a.NB = (N + kGroup - 1) / kGroup;
+    a.wait_ns = tile_wait_limit_ns();
+    a.withhold = tile_withhold_first_load() ? 1 : 0;
     // 256-wide weight tiles when the grid is large (prefill: fewer operand
     // re-reads per FLOP); 128-wide ones otherwise (twice the tiles to spread
     // a batched-decode weight stream over the SMs).

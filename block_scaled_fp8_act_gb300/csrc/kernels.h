@@ -68,8 +68,26 @@ cudaError_t launch_linear_fused(const void* x, const uint8_t* w, const float* sw
 cudaError_t launch_gemm_tc(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N, int K,
                            void* out, bool out_f32, int num_sms, cudaStream_t stream);
 
-// Device-side error word of the tcgen05 kernel (non-zero after a bounded
-// wait gave up); reading it synchronises with the device and clears it.
+// Weight-streaming tcgen05 GEMM for small batched decode, kMidMaxM >= M > 16:
+// 128 weight rows x round16(M) tokens per tile (swap-AB), TMA-fed ring, the
+// block scales promoted per K group, split K over a thread-block cluster
+// when the tiles are fewer than the SMs. Returns cudaErrorNotSupported
+// (launching nothing) when a CTA's scale table would not fit its shared
+// memory (very long K on few tiles).
+constexpr int kMidMaxM = 48;   // measured: ahead of the token-tiled kernel up to 48 tokens, behind above 64
+constexpr int kMidMaxTokens = 128;  // the kernel itself handles up to 128
+cudaError_t launch_gemm_midm(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N,
+                             int K, void* out, bool out_f32, int num_sms, cudaStream_t stream);
+
+// Device-side error words of the tcgen05 kernels (non-zero after a bounded
+// wait gave up); reading one synchronises with the device and clears it.
 unsigned int read_and_clear_tc_error();
+unsigned int read_and_clear_midm_error();
+
+// Launch arguments of the tcgen05 kernels' failure path, set process-wide by
+// the fp8act_set_wait_limit() test hook: the wall-time bound of every wait
+// that may give up, and whether each CTA withholds its first operand copy.
+unsigned long long tile_wait_limit_ns();
+bool tile_withhold_first_load();
 
 }  // namespace fp8act

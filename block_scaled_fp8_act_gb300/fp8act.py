@@ -63,11 +63,12 @@ def load(build: bool = False) -> ctypes.CDLL:
     L.fp8act_strerror.argtypes = [i]
     L.fp8act_strerror.restype = ctypes.c_char_p
     L.fp8act_check_status.argtypes = [p]
+    L.fp8act_set_wait_limit.argtypes = [ctypes.c_longlong, i]
     for fn in (L.fp8_act_quant, L.fp8_weight_quant, L.fp8_block_gemm, L.fp8_block_gemm_f32,
                L.fp8_block_gemm_w8a16, L.fp8_block_gemm_w8a16_f32,
                L.fp8_act_quant_grouped, L.fp8_block_gemm_grouped, L.fp8_block_gemm_grouped_f32,
                L.fp8_linear, L.fp8_linear_f32,
-               L.fp8act_check_status, L.fp8act_version):
+               L.fp8act_check_status, L.fp8act_set_wait_limit, L.fp8act_version):
         fn.restype = ctypes.c_int
     _lib = L
     return L
@@ -272,3 +273,10 @@ def fp8_block_gemm_grouped_f32(problems, outs=None, stream=None) -> list:
 def check_status(stream=None) -> int:
     """Synchronise the stream and return the library's device-side status."""
     return int(load().fp8act_check_status(_stream(stream)))
+
+
+def set_wait_limit(limit_ns: int, withhold_first_load: bool = False) -> None:
+    """Test hook of the tcgen05 kernels' failure path (see fp8act_set_wait_limit):
+    the wall-time bound of their waits (negative = the 2 s default) and whether
+    each CTA skips its first operand copy."""
+    _check("fp8act_set_wait_limit", load().fp8act_set_wait_limit(int(limit_ns), 1 if withhold_first_load else 0))

@@ -83,12 +83,28 @@ FP8ACT_API int fp8_weight_quant(const void* w_bf16, int N, int K, void* w_e4m3, 
 
 /*
  * Block-scaled GEMM: out[M, N] = bf16(y) with y as defined above, fp32
- * accumulation. Dispatches on M: for M <= 16 a weight-streaming kernel over
- * 16-row weight tiles (each tile's whole K on one SM, summed in a fixed
- * order, so results are bit-reproducible); larger M take tile kernels.
- * Every M >= 1 is supported. Kernels launch with programmatic dependent
- * launch: the weight stream starts before the previous kernel on the stream
- * has finished, and activations are read only after it has.
+ * accumulation. Dispatches on M:
+ *   M <= 16      a weight-streaming kernel over 16-row weight tiles on the
+ *                warp-level tensor-core MMA (decode and speculative verify);
+ *   16 < M <= 48 a weight-streaming tcgen05 kernel: 128 weight rows x
+ *                round16(M) tokens per tile (swap-AB), K split over a
+ *                thread-block cluster when the tiles are fewer than the SMs;
+ *   M > 48       tcgen05 tiles of 128 tokens x 128 / 256 weight rows (batched
+ *                decode, "高并发优化" of the smartx.com Qwen3.8-27B post, and
+ *                prefill), K split over a cluster when the tiles are few.
+ *   (The boundary at 48 is measured: ahead below it, behind from 64.)
+ * Every M >= 1 is supported and every kernel sums in a fixed order, so
+ * results are bit-reproducible for a given M, N, K.
+ *
+ * Ordering (programmatic dependent launch): each kernel may start while the
+ * kernel before it on the stream is still running; it reads the activation
+ * codes and scales, and writes `out`, only after that kernel has completed,
+ * but it starts reading w and sw at once. The weights and weight scales must
+ * therefore be complete before the previous kernel on the stream starts (an
+ * fp8_act_quant launch lets the GEMM after it start immediately): write them
+ * on another stream or earlier and synchronise (an event or
+ * cudaStreamSynchronize) before the chain that reads them, as a served
+ * model's loaded checkpoint is.
  *   q_e4m3, sa : activation codes [M, K] and scales [M, K/128]
  *   w_e4m3, sw : weight codes [N, K] and scales [ceil(N/128), K/128]
  *   out_bf16   : [M, N] bf16 out
@@ -199,10 +215,29 @@ FP8ACT_API const char* fp8act_strerror(int status);
 /*
  * Synchronises `stream` and reports whether any kernel of this library on the
  * current device gave up a bounded wait since the last call (FP8ACT_ERR_TIMEOUT),
- * then clears the flag. Returns FP8ACT_ERR_CUDA if the stream itself failed.
+ * then clears the flag. The flag is one word per device, shared by every
+ * stream: a timeout in a kernel on another stream is reported here too (and
+ * cleared), and work still running on other streams may set it after the
+ * call returns. Returns FP8ACT_ERR_CUDA if the stream itself failed.
  * Not capturable (it synchronises); meant for tests and health checks.
  */
 FP8ACT_API int fp8act_check_status(void* stream);
+
+/*
+ * Test hook for the failure path of the tcgen05 kernels (M > 16). Every wait
+ * of those kernels on a barrier that another role completes is bounded by
+ * wall time (2 s by default); on expiry the CTA stops issuing work, waits for
+ * the copies and MMAs it has already issued, frees its tensor memory, leaves,
+ * and fp8act_check_status() reports FP8ACT_ERR_TIMEOUT.
+ *   limit_ns            bound of those waits for launches issued after this
+ *                       call; a negative value restores the 2 s default
+ *   withhold_first_load non-zero: every CTA of those launches skips its first
+ *                       operand copy, so that its first wait runs out
+ *                       (the GEMM's output is then undefined)
+ * Process-wide; not for production use (a CUDA graph captured meanwhile
+ * keeps the values it was captured with). Always returns FP8ACT_OK.
+ */
+FP8ACT_API int fp8act_set_wait_limit(long long limit_ns, int withhold_first_load);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 FP8ACT_API int fp8act_version(void);

@@ -13,6 +13,8 @@ Tolerances (fixed by the layer's definition, not tuned):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -21,6 +23,10 @@ from block_scaled_fp8_act_gb300 import inputs
 
 G = 128
 REL_L2_TOL = 1e-4
+
+# Every compare_gemm result of the session (test id, shape, statistics); the
+# conftest prints them at the end of the run.
+STATS: list = []
 
 
 def bf16_ordinal(bits: np.ndarray) -> np.ndarray:
@@ -54,8 +60,12 @@ def compare_gemm(out_bf16: torch.Tensor, out_f32: torch.Tensor, y: np.ndarray, a
     bad = (dist > 1) & ~floor_ok
     assert not bad.any(), (f"{int(bad.sum())} elements beyond 1 bf16 ulp and the fp32 bound; first at "
                            f"{np.argwhere(bad)[0]}: gpu {gf[bad][0]!r} ref {y[bad][0]!r}")
-    return {"rel_l2": float(rel), "max_ulp": int(dist.max()) if dist.size else 0,
-            "floor_used": int(((dist > 1) & floor_ok).sum()), "exact_bf16": float((dist == 0).mean()) if dist.size else 1.0}
+    stats = {"rel_l2": float(rel), "max_ulp": int(dist.max()) if dist.size else 0,
+             "floor_used": int(((dist > 1) & floor_ok).sum()), "elements": int(dist.size),
+             "exact_bf16": float((dist == 0).mean()) if dist.size else 1.0}
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    STATS.append({"test": test, "rows": int(y.shape[0]), "N": int(y.shape[1]), "K": int(K), **stats})
+    return stats
 
 
 class Problem:
@@ -84,11 +94,40 @@ class Problem:
         out = fp8act.fp8_block_gemm(q, sa, self.w, self.sw)
         out32 = fp8act.fp8_block_gemm_f32(q, sa, self.w, self.sw)
         torch.cuda.synchronize()
-        y, aabs, ref = oracle.block_gemm(q_ref, sa_ref, self.w_ref, self.sw_ref, rows=rows)
+        y, aabs, ref = oracle_gemm(q_ref, sa_ref, self.w_ref, self.sw_ref, rows=rows)
         if rows is not None:
             idx = torch.as_tensor(np.asarray(rows), device=out.device)
             out, out32 = out.index_select(0, idx), out32.index_select(0, idx)
         return compare_gemm(out, out32, y, aabs, ref, self.K)
+
+
+def oracle_gemm(q, sa, w, sw, rows=None, chunk: int = 256):
+    """oracle.block_gemm over whole 128-row weight blocks at a time,
+    concatenated along N: the same definition, on sub-problems whose weights
+    stay in a host core's cache while every sampled row passes over them."""
+    N = w.shape[0]
+    if N <= chunk:
+        return oracle.block_gemm(q, sa, w, sw, rows=rows)
+    parts = [oracle.block_gemm(q, sa, w[n0:n0 + chunk], sw[n0 // G:(n0 + chunk + G - 1) // G], rows=rows)
+             for n0 in range(0, N, chunk)]
+    return tuple(np.concatenate([p[i] for p in parts], axis=1) for i in range(3))
+
+
+def tile_rows(M: int, n_random: int, seed: int, edge: int = 128) -> np.ndarray:
+    """Rows of an M-token GEMM to compare against the oracle: the first and
+    last `edge` rows, a seeded random row of every 32-row lane quadrant of
+    every 128-row token tile (m = 128 t + 32 q + r: every tile and every
+    tensor-memory lane group of the token-tiled kernel), and `n_random`
+    seeded random rows."""
+    rng = np.random.default_rng(seed)
+    rows = set(range(min(edge, M))) | set(range(max(0, M - edge), M))
+    for t in range((M + 127) // 128):
+        for qd in range(4):
+            lo = 128 * t + 32 * qd
+            if lo < M:
+                rows.add(int(lo + rng.integers(0, min(32, M - lo))))
+    rows |= set(rng.choice(M, size=min(n_random, M), replace=False).tolist())
+    return np.array(sorted(rows), np.int64)
 
 
 def sample_rows(M: int, n_random: int, seed: int) -> np.ndarray:

@@ -98,8 +98,12 @@ def test_gemm_batched_decode(fp8act, si, M):
 
 @pytest.mark.parametrize("si", range(len(SHAPES)))
 def test_gemm_prefill_sampled_rows(fp8act, si):
-    from parity_util import sample_rows
-    rows = sample_rows(4096, 24, seed=si)
+    """M = 4096 on every projection shape, on every output column of about
+    640 rows: the first and last 128, one random row in each 32-row lane
+    quadrant of each of the 32 token tiles, and 256 random rows."""
+    from parity_util import tile_rows
+    rows = tile_rows(4096, 256, seed=si)
+    assert len(rows) >= 256 + 2 * 128
     problem(si).run_and_compare(4096, inputs.activation_seed(si, 10), rows=rows)
 
 
@@ -108,9 +112,49 @@ def test_gemm_prefill_ragged_n(fp8act, N, K):
     """M = 4096 with N past the last full 256-wide tile: the last tile's rows
     beyond N read as zero, its scale blocks end inside the tile, and nothing
     is stored past N."""
-    from parity_util import Problem, sample_rows
-    rows = sample_rows(4096, 24, seed=N)
+    from parity_util import Problem, tile_rows
+    rows = tile_rows(4096, 256, seed=N)
     Problem(N, K, seed=N + K).run_and_compare(4096, seed=7, rows=rows)
+
+
+def test_gemm_prefill_ragged_n_writes_nothing_outside_out(fp8act):
+    """The persistent 256-wide store path with N = 2600 (the last tile ends
+    40 rows past N): canaries on both sides of the output stay intact."""
+    from parity_util import Problem
+    p = Problem(2600, 1024, seed=2600 + 1024)
+    M = 4096
+    q, sa, _, _ = p.activations(M, seed=5)
+    pad = 1 << 16
+    for dtype, call in ((torch.bfloat16, fp8act.fp8_block_gemm), (torch.float32, fp8act.fp8_block_gemm_f32)):
+        buf = torch.full((M * p.N + 2 * pad,), -7.0, dtype=dtype, device="cuda")
+        out = buf[pad:pad + M * p.N].view(M, p.N)
+        call(q, sa, p.w, p.sw, out)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:pad] == -7.0) and torch.all(buf[pad + M * p.N:] == -7.0), dtype
+        assert torch.all(torch.isfinite(out.float()))
+
+
+# ------------------------------------------- batched decode (16 < M <= 128)
+@pytest.mark.parametrize("M", [17, 24, 33, 48, 49, 80, 96, 113, 128])
+@pytest.mark.parametrize("N,K", [(1000, 2048), (300, 640), (2176, 1152)])
+def test_gemm_midm_widths_and_splits(fp8act, M, N, K):
+    """Batched-decode widths on both sides of the kernel boundary (the
+    weight-streaming tcgen05 kernel up to 48 tokens, its token tiles 32 and
+    48 wide; the token-tiled kernel from 49) against N that ends inside a
+    weight tile and K split over clusters of 2 .. 8 CTAs (N = 1000: 8 tiles,
+    16 K groups; N = 300: 3 tiles, 5 K groups; N = 2176: 17 tiles, 9 K
+    groups)."""
+    from parity_util import Problem
+    Problem(N, K, seed=N + K + 1).run_and_compare(M, seed=M + 11)
+
+
+@pytest.mark.parametrize("M", [32, 102])
+def test_gemm_midm_many_tiles_per_cta(fp8act, vocab_problem, M):
+    """The vocabulary-sized head at batched-decode widths: 1187 weight tiles
+    on at most one CTA per SM, so every CTA walks several tiles (the
+    persistent path of both tile kernels: the accumulator ring runs on
+    across tiles)."""
+    vocab_problem.run_and_compare(M, seed=720 + M)
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 17, 128), (3, 200, 256), (8, 1000, 384), (9, 130, 512),
@@ -540,3 +584,4 @@ def test_act_quant_bit_exact_over_many_scales(fp8act):
     q_ref, sa_ref = oracle.act_quant(inputs.bf16_bits(xb))
     assert np.array_equal(sa.cpu().numpy(), sa_ref)
     assert np.array_equal(q.cpu().numpy(), q_ref)
+
