@@ -265,7 +265,7 @@ const char* fp8act_strerror(int status) {
         case FP8ACT_ERR_NULL: return "a required pointer is NULL";
         case FP8ACT_ERR_SHAPE:
             return "bad shape: M, N must be >= 0 and K a positive multiple of 128 (grouped calls: at most 16 "
-                   "problems; fp8_linear: min(8, M) rows of K codes must fit in 200 KiB)";
+                   "problems; fp8_linear: min(8, M) rows of K codes and scales must fit in 200 KiB)";
         case FP8ACT_ERR_ALIGN: return "misaligned pointer: tensors need 16-byte, scales 4-byte alignment";
         case FP8ACT_ERR_LAUNCH: return "kernel launch failed";
         case FP8ACT_ERR_TIMEOUT: return "a kernel gave up a bounded wait (device-side timeout)";

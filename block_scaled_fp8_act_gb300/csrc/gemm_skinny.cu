@@ -46,10 +46,12 @@
 // Fused mode (kModeFQ): bf16 activations in, the layer's full W8A8 result
 // out, in one launch (the quantisation launch per linear layer is what the
 // same post's single-request section credits the weight-only back-end with
-// saving; here the quantisation stays and moves into the GEMM). After the
-// programmatic-launch wait each CTA quantises its <= 8 tokens into shared
-// memory with the activation kernel's own group code (so the codes and
-// scales are the same bits), then runs the W8A8 loop on them. Every CTA
+// saving; here the quantisation stays and moves into the GEMM). Each warp
+// quantises, step by step, exactly the 1x128 groups of the K blocks it
+// multiplies (its <= 8 tokens), with the activation kernel's own group code
+// (the same codes and scales bit for bit), into a 1 KB slice of shared memory
+// per block, right after its weight loads for the step are in flight: no
+// warp waits for another and the weight stream never stops. Every CTA
 // repeats the quantisation of the same tokens, so the mode suits small M.
 #include <atomic>
 
@@ -66,7 +68,7 @@ namespace {
 constexpr int kMaxWarps = 16;
 // Kernel modes: W8A8 (E4M3 activation codes and scales in), weight-only
 // (bf16 activations, widened weights) and fused (bf16 activations quantised
-// by the CTA into shared memory, then the W8A8 loop).
+// by each warp into shared memory, then the W8A8 loop).
 constexpr int kModeW8A8 = 0;
 constexpr int kModeA16 = 1;
 constexpr int kModeFQ = 2;
@@ -76,7 +78,13 @@ constexpr int kModeFQ = 2;
 constexpr int kWideBit = 4;
 constexpr int base_mode(int mode) { return mode & 3; }
 constexpr bool wide_mode(int mode) { return (mode & kWideBit) != 0; }
-constexpr size_t kFusedMaxSmem = 200 * 1024;  // the fused mode's shared-memory ceiling per CTA
+// Fused mode: each warp's shared-memory slice holds the codes [J][rows][128]
+// and scales [J][rows] of the J = ceil(KB / warps) K blocks it multiplies
+// (kb = warp, warp + warps, ...), rows = min(8, M) tokens.
+constexpr size_t kFqMaxSmem = 200 * 1024;  // the fused slices of one CTA, at most
+__host__ __device__ constexpr int fq_slice_bytes(int KB, int warps, int rows) {
+    return ((KB + warps - 1) / warps * rows * (kGroup + 4) + 15) & ~15;
+}
 // L2 prefetch distance, in warp steps: each warp keeps the weight lines of
 // the next steps on their way into L2 (prefetches hold no registers). One
 // step measured best: 10% off the five decode shapes at M = 1 against no
@@ -129,8 +137,8 @@ __device__ __forceinline__ void widen_row(const uint4& lo, const uint4& hi, uint
 // kTG = groups of 8 tokens a CTA handles (they share the weight fragments);
 // kMode: kModeW8A8 (codes in `q`, scales in `sa`), kModeA16 (bf16
 // activations in `q`, `sa` unused) or kModeFQ (bf16 activations in `q`,
-// quantised into the dynamic shared memory `fq_smem`: min(8, M) rows of K
-// codes, then their K / 128 scales; `sa` unused; kTG must be 1).
+// quantised by each warp, step by step, into its slice of the dynamic shared
+// memory `fq_smem`; `sa` unused; kTG must be 1).
 template <bool kF32Out, int kUnroll, int kTG, int kMode>
 __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const float* __restrict__ sa,
                                             const uint8_t* __restrict__ w, const float* __restrict__ sw, int M,
@@ -174,7 +182,7 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
     const uint8_t* w_pf = w + static_cast<int64_t>(n0 + lane) * K;
     if (pf_lane) {
 #pragma unroll
-        for (int s = base_mode(kMode) == kModeFQ ? 0 : 1; s <= kL2Ahead; ++s)
+        for (int s = 1; s <= kL2Ahead; ++s)
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int kb = warp + s * stride + u * nwarps;
@@ -182,37 +190,15 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
             }
     }
     bool waited = false;
+    // Fused mode: this warp's private slice of the dynamic shared memory holds
+    // the codes and scales of the K blocks it multiplies (slot j: block
+    // warp + j * nwarps), quantised by the warp itself once its first weight
+    // loads are in flight.
+    const int fq8 = M < 8 ? M : 8;  // token rows of every slot (the slice size is per launch)
     const int fq_rows = M - m0 < 8 ? M - m0 : 8;
-    const uint8_t* q_s = fq_smem;
-    const float* sa_s = reinterpret_cast<const float*>(fq_smem + static_cast<int64_t>(fq_rows) * K);
-    if constexpr (base_mode(kMode) == kModeFQ) {
-        // Quantise this CTA's tokens m0 .. m0 + fq_rows - 1 into shared memory:
-        // half-warp h of warp w takes groups 2 w + h, 2 w + h + 2 nwarps, ...
-        // (row-major over (token, K group)); the whole warp runs every pass
-        // because the group code shuffles across the warp.
-        ptx::griddep_wait();
-        waited = true;
-        uint8_t* q_w = fq_smem;
-        float* sa_w = reinterpret_cast<float*>(fq_smem + static_cast<int64_t>(fq_rows) * K);
-        const int half = lane >> 4;
-        const int hl = lane & 15;
-        const int groups = fq_rows * KB;
-        for (int base = 2 * warp; base < groups; base += 2 * nwarps) {
-            const int gi = base + half;
-            const bool ok = gi < groups;
-            const int r = ok ? gi / KB : 0;
-            const int kb = ok ? gi % KB : 0;
-            const uint4 v = ok ? ld_dep_stream_v4(q + (static_cast<int64_t>(m0 + r) * K + kb * kGroup + 8 * hl) * 2)
-                               : zero;
-            uint2 codes;
-            const float sg = quant_group_halfwarp(v, codes);
-            if (ok) {
-                *reinterpret_cast<uint2*>(q_w + static_cast<int64_t>(r) * K + kb * kGroup + 8 * hl) = codes;
-                if (hl == 0) sa_w[r * KB + kb] = sg;
-            }
-        }
-        __syncthreads();
-    }
+    const int fq_slots = (KB + nwarps - 1) / nwarps;
+    uint8_t* const q_s = fq_smem + static_cast<int64_t>(warp) * fq_slice_bytes(KB, nwarps, fq8);
+    float* const sa_s = reinterpret_cast<float*>(q_s + fq_slots * fq8 * kGroup);
     for (int kb0 = warp; kb0 < KB; kb0 += stride) {
         if (pf_lane) {
 #pragma unroll
@@ -241,6 +227,31 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
         if (!waited) {
             ptx::griddep_wait();
             waited = true;
+            if constexpr (base_mode(kMode) == kModeFQ) {
+                // Quantise every 1x128 group (token r, block kb) this warp will multiply,
+                // with the activation kernel's group code (the same codes and scales bit
+                // for bit): half-warp h takes groups 2 p + h of pass p, and the whole warp
+                // runs every pass because the group code shuffles. The first step's
+                // weight loads are already in flight and no other warp waits for it.
+                const int half = lane >> 4;
+                const int hl = lane & 15;
+                const int groups = fq_slots * fq_rows;
+                for (int base_g = 0; base_g < groups; base_g += 2) {
+                    const int gi = base_g + half;
+                    const int j = gi / fq_rows, r = gi % fq_rows;
+                    const int kb = warp + j * nwarps;
+                    const bool ok = gi < groups && kb < KB;
+                    const uint4 v = ok ? ld_dep_stream_v4(q + (static_cast<int64_t>(m0 + r) * K + kb * kGroup + 8 * hl) * 2)
+                                       : zero;
+                    uint2 codes;
+                    const float sg = quant_group_halfwarp(v, codes);
+                    if (ok) {
+                        *reinterpret_cast<uint2*>(q_s + (j * fq8 + r) * kGroup + 8 * hl) = codes;
+                        if (hl == 0) sa_s[j * fq8 + r] = sg;
+                    }
+                }
+                __syncwarp();
+            }
         }
         if constexpr (base_mode(kMode) == kModeA16) {
 #pragma unroll
@@ -282,8 +293,9 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
             for (int j = 0; j < kTG; ++j) {
                 const int m = m0 + 8 * j + g;  // this lane's token for the B fragment
                 const bool ok_x = m < M;
-                const uint8_t* x_r = base_mode(kMode) == kModeFQ ? q_s + static_cast<int64_t>(g) * K + lane_off
+                const uint8_t* x_r = base_mode(kMode) == kModeFQ ? q_s + g * kGroup + lane_off
                                                                  : q + static_cast<int64_t>(m) * K + lane_off;
+                const int j0 = (kb0 - warp) / nwarps;  // fused mode: slot of this step's first block
                 constexpr int kHiOff = kWide ? 16 : 64;  // byte offset of the lane's second 16 bytes
                 const int c0 = m0 + 8 * j + 2 * t;  // token columns of this lane's accumulators
                 uint4 xlo[kUnroll], xhi[kUnroll];
@@ -293,8 +305,9 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                     const bool ok_k = kb < KB;
                     const int64_t off = static_cast<int64_t>(kb) * kGroup;
                     if constexpr (base_mode(kMode) == kModeFQ) {
-                        xlo[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + off) : zero;
-                        xhi[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + off + kHiOff) : zero;
+                        const int so = (j0 + u) * fq8 * kGroup;  // slot of block u of this step
+                        xlo[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + so) : zero;
+                        xhi[u] = (ok_k && ok_x) ? *reinterpret_cast<const uint4*>(x_r + so + kHiOff) : zero;
                     } else if constexpr (kWide) {
                         xlo[u] = xhi[u] = zero;
                         if (ok_k && ok_x) ld_dep_v8(x_r + off, xlo[u], xhi[u]);
@@ -315,8 +328,8 @@ __device__ __forceinline__ void skinny_tile(const uint8_t* __restrict__ q, const
                         const float s_w = __ldg(sw_r + kb);
                         float sa0 = 0.f, sa1 = 0.f;
                         if constexpr (base_mode(kMode) == kModeFQ) {
-                            if (c0 < M) sa0 = sa_s[(c0 - m0) * KB + kb];
-                            if (c0 + 1 < M) sa1 = sa_s[(c0 + 1 - m0) * KB + kb];
+                            if (c0 < M) sa0 = sa_s[(j0 + u) * fq8 + (c0 - m0)];
+                            if (c0 + 1 < M) sa1 = sa_s[(j0 + u) * fq8 + (c0 + 1 - m0)];
                         } else {
                             if (c0 < M) sa0 = ld_dep_f32(sa + static_cast<int64_t>(c0) * KB + kb);
                             if (c0 + 1 < M) sa1 = ld_dep_f32(sa + static_cast<int64_t>(c0 + 1) * KB + kb);
@@ -399,32 +412,49 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_grouped_kernel(con
                                             (local / p.tiles_n) * 8, red);
 }
 
-// Dynamic shared memory of the fused mode: min(8, M) rows of K codes and of
-// K / 128 fp32 scales.
-size_t fused_smem_bytes(int M, int K) {
-    const size_t rows = M < 8 ? M : 8;
-    return rows * (static_cast<size_t>(K) + 4 * static_cast<size_t>(K / kGroup));
-}
-
-// CTAs per SM for a (load depth, token groups, warps) configuration, from the
-// occupancy API; cached per device when the CTA uses no dynamic shared memory.
+// CTAs per SM for a (load depth, token groups, mode, warps) configuration
+// without dynamic shared memory, from the occupancy API (cached per device).
 template <bool kF32Out, int kUnroll, int kTG, int kMode>
-int ctas_per_sm(int wv, size_t smem) {
+int ctas_per_sm(int wv) {
     static std::atomic<int> cache[64][kMaxWarps + 1];  // 0 = unknown, else 1 + CTAs per SM
     int dev = 0;
     cudaGetDevice(&dev);
-    int cached = smem == 0 ? cache[dev & 63][wv].load(std::memory_order_relaxed) : 0;
+    int cached = cache[dev & 63][wv].load(std::memory_order_relaxed);
     if (cached == 0) {
         int per_sm = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_skinny_kernel<kF32Out, kUnroll, kTG, kMode>,
-                                                          32 * wv, smem) != cudaSuccess) {
+                                                          32 * wv, 0) != cudaSuccess) {
             cudaGetLastError();
             per_sm = 0;
         }
         cached = per_sm + 1;
-        if (smem == 0) cache[dev & 63][wv].store(cached, std::memory_order_relaxed);
+        cache[dev & 63][wv].store(cached, std::memory_order_relaxed);
     }
     return cached - 1;
+}
+
+// CTAs per SM that the SM's shared memory allows with `smem` dynamic bytes
+// per CTA (and the 1 KB the runtime reserves per CTA).
+int smem_ctas_per_sm(size_t smem) {
+    if (smem == 0) return 1 << 20;
+    static std::atomic<int> per_sm_bytes[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int b = per_sm_bytes[dev & 63].load(std::memory_order_relaxed);
+    if (b == 0) {
+        if (cudaDeviceGetAttribute(&b, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            b = 228 * 1024;
+        }
+        per_sm_bytes[dev & 63].store(b, std::memory_order_relaxed);
+    }
+    return static_cast<int>(static_cast<size_t>(b) / (smem + 1024));
+}
+
+// Dynamic shared memory of a CTA with wv warps: the fused mode's slices.
+template <int kMode>
+size_t cta_smem(int KB, int wv, int M) {
+    return base_mode(kMode) == kModeFQ ? static_cast<size_t>(wv) * fq_slice_bytes(KB, wv, M < 8 ? M : 8) : 0;
 }
 
 // Warps per CTA for a load depth: among the warp counts whose K groups split
@@ -432,14 +462,19 @@ int ctas_per_sm(int wv, size_t smem) {
 // which the whole grid is resident in one wave, the one with the most weight
 // bytes in flight (capped where HBM saturates, ~20 MB on GB300); 0 if none.
 template <bool kF32Out, int kUnroll, int kTG, int kMode = kModeW8A8>
-int pick_warps(int64_t ctas, int KB, int num_sms, int64_t* inflight_out, size_t smem = 0) {
+int pick_warps(int64_t ctas, int KB, int num_sms, int64_t* inflight_out, int M = 1) {
     constexpr int64_t kSaturate = int64_t(20) << 20;
     int best = 0;
     int64_t best_inflight = -1;
     for (int wv = 1; wv <= kMaxWarps && wv <= KB; ++wv) {
         const int per_warp = (KB + wv - 1) / wv;
         if (10 * KB < 9 * wv * per_warp) continue;  // warps would finish more than 10% apart
-        if (ctas > static_cast<int64_t>(ctas_per_sm<kF32Out, kUnroll, kTG, kMode>(wv, smem)) * num_sms) continue;
+        const size_t smem = cta_smem<kMode>(KB, wv, M);
+        if (smem > kFqMaxSmem) continue;
+        int per_sm = ctas_per_sm<kF32Out, kUnroll, kTG, kMode>(wv);
+        const int by_smem = smem_ctas_per_sm(smem);
+        if (by_smem < per_sm) per_sm = by_smem;
+        if (ctas > static_cast<int64_t>(per_sm) * num_sms) continue;
         int64_t inflight = ctas * wv * (per_warp < kUnroll ? per_warp : kUnroll) * (16 * kGroup);
         if (inflight > kSaturate) inflight = kSaturate;
         if (inflight > best_inflight || (inflight == best_inflight && wv < best)) {
@@ -459,8 +494,7 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
     const int64_t ctas = static_cast<int64_t>(grid.x) * grid.y;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    // The fused mode keeps min(8, M) rows of codes and scales in dynamic shared memory.
-    const size_t smem = base_mode(kMode) == kModeFQ ? fused_smem_bytes(M, K) : 0;
+    // The fused mode gives each warp a slice of dynamic shared memory.
     if constexpr (base_mode(kMode) == kModeFQ) {
         static std::atomic<uint64_t> configured{0};  // one bit per device
         int dev = 0;
@@ -469,15 +503,18 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
         if (!(configured.load(std::memory_order_acquire) & bit)) {
             const cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<kF32Out, kUnroll, kTG, kMode>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       static_cast<int>(kFusedMaxSmem));
+                                                       static_cast<int>(kFqMaxSmem));
             if (e != cudaSuccess) return e;
             configured.fetch_or(bit, std::memory_order_release);
         }
     }
-    int wv = pick_warps<kF32Out, kUnroll, kTG, kMode>(ctas, KB, num_sms, nullptr, smem);
+    int wv = pick_warps<kF32Out, kUnroll, kTG, kMode>(ctas, KB, num_sms, nullptr, M);
     if (wv == 0) wv = KB < 4 ? KB : 4;  // grid larger than one wave: plain 4-warp CTAs
+    // the fused slices of very long K at wide M: more warps, smaller slices
+    while (cta_smem<kMode>(KB, wv, M) > kFqMaxSmem && wv < kMaxWarps && wv < KB) ++wv;
+    if (cta_smem<kMode>(KB, wv, M) > kFqMaxSmem) return cudaErrorInvalidValue;
     cfg.blockDim = dim3(32 * wv);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = cta_smem<kMode>(KB, wv, M);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -597,7 +634,12 @@ cudaError_t launch_gemm_skinny_grouped(const GemmProblem* probs, int count, bool
                    : cudaLaunchKernelEx(&cfg, gemm_skinny_grouped_kernel<false, 1>, args);
 }
 
-bool fused_fits(int M, int K) { return fused_smem_bytes(M, K) <= kFusedMaxSmem; }
+bool fused_fits(int M, int K) {
+    // the slices of any warp count hold every block once, plus at most 15
+    // bytes of rounding per warp
+    const int KB = K / kGroup;
+    return static_cast<size_t>(KB) * (M < 8 ? M : 8) * (kGroup + 4) + 15 * kMaxWarps <= kFqMaxSmem;
+}
 
 cudaError_t launch_linear_fused(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
                                 bool out_f32, int num_sms, cudaStream_t stream) {
