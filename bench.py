@@ -84,6 +84,8 @@ def gemm_kernel_name(M: int) -> str:
 WEIGHT_COPIES = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+NOMINAL_HBM_GBS = 7900.0     # GB300 HBM3e, nominal
+NOMINAL_FP8_TFLOPS = 4500.0  # GB300 dense FP8, nominal
 
 
 # ------------------------------------------------------------------ helpers
@@ -372,6 +374,16 @@ def gemm_kernel_times(wl: Workload, stream, launches: int = 60, reps: int = 7, s
     return [med for med, _, _ in res]
 
 
+def floor_times(wl: Workload, stream, launches: int = 60, reps: int = 7) -> list[float]:
+    """The streaming-read floor of each shape's weight stream: a chain of plain
+    reads of the same (rotating) weight copies, launched like the GEMMs."""
+    from block_scaled_fp8_act_gb300 import fp8act
+    sink = torch.zeros(1, dtype=torch.int32, device=wl.out_all.device)
+    res = chain_times([lambda i, si=si: fp8act.stream_read(wl.w[si][i % wl.copies], sink, stream=stream)
+                       for si in range(len(wl.shapes))], stream, launches, reps)
+    return [med for med, _, _ in res]
+
+
 def quant_kernel_times(wl: Workload, stream, launches: int = 60, reps: int = 7) -> list[tuple[float, float, float]]:
     """The activation-quantisation launch of each shape, timed like the GEMMs."""
     from block_scaled_fp8_act_gb300 import fp8act
@@ -512,26 +524,22 @@ def run_reference(args, world: int, rank: int) -> None:
 
 
 def sweep(weights, device, stream, peaks) -> dict:
-    """us/call of the block GEMM per shape at every workload M (outside the timed step)."""
-    res = {}
+    """us/call of the block GEMM per shape at every workload M (outside the
+    timed step), compact: per M the five us/call and the fraction of the
+    roofline (HBM up to M = 102, FP8 tensor peak at 4096; burst peaks, each
+    GEMM runs alone)."""
+    res = {"shapes": [list(sh) for sh in weights.shapes], "us": {}, "frac": {}}
     hbm = peaks["hbm_gbs"]
-    fp8_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP8_OVER_BF16
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     for M in (1, 2, 3, 4, 5, 6, 7, 8, 64, 102, 4096):
         wl = Workload(M, weights, device)
         ts = gemm_kernel_times(wl, stream, launches=30 if M <= 102 else 3, reps=3)
-        row = []
-        for (N, K), t in zip(wl.shapes, ts):
-            e = {"N": N, "K": K, "us": round(t * 1e6, 3)}
-            if M <= 102:
-                gbs = algorithmic_gemm_bytes(M, N, K) / t / 1e9
-                e["gbs"] = round(gbs, 1)
-                e["frac_hbm"] = round(gbs / hbm, 4)
-            else:
-                tf = 2.0 * M * N * K / t / 1e12
-                e["tflops"] = round(tf, 1)
-                e["frac_fp8"] = round(tf / fp8_peak, 4)
-            row.append(e)
-        res[str(M)] = row
+        res["us"][str(M)] = [round(t * 1e6, 2) for t in ts]
+        if M <= 102:
+            fr = [algorithmic_gemm_bytes(M, N, K) / t / 1e9 / hbm for (N, K), t in zip(wl.shapes, ts)]
+        else:
+            fr = [2.0 * M * N * K / t / 1e12 / fp8_peak for (N, K), t in zip(wl.shapes, ts)]
+        res["frac"][str(M)] = [round(f, 3) for f in fr]
         del wl
         torch.cuda.empty_cache()
     return res
@@ -550,6 +558,10 @@ def main() -> None:
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode",
                     help="decode (M=1, the headline), verify, batched or prefill")
     ap.add_argument("--m", type=int, default=None, help="token count for the chosen workload")
+    ap.add_argument("--floor", action="store_true",
+                    help="also time the streaming-read floor of each shape's weights (diagnostic)")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="extra timed repetitions of the K steps, reported as min / median / max")
     ap.add_argument("--steps-per-graph", type=int, default=10,
                     help="consecutive steps captured in one CUDA graph (timed steps stay exactly --steps)")
     args = ap.parse_args()
@@ -620,6 +632,16 @@ def main() -> None:
         torch.cuda.synchronize()
         barrier(world)
         t_step = start.elapsed_time(end) / 1e3 / args.steps
+        # the same K steps again, args.repeats times, for the spread
+        rep_ms = []
+        for _ in range(args.repeats):
+            r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                r0.record(stream)
+                replay_steps(args.steps)
+                r1.record(stream)
+            r1.synchronize()
+            rep_ms.append(r0.elapsed_time(r1) / args.steps)
         # dominant kernel: the block GEMM, timed per shape on the same stream
         gemm_spread = []
         gemm_ts = gemm_kernel_times(wl, stream, launches=60 if M <= 128 else 8, spread=gemm_spread)
@@ -691,6 +713,12 @@ def main() -> None:
                       "frac": round(b / t / 1e9 / peak, 4)}
                      for lb, t, b, (lo, hi) in zip(labels, gemm_ts, gemm_bytes, gemm_spread)]
 
+    floor = None
+    if args.floor and not wl.grouped:
+        fts = floor_times(wl, stream)
+        floor = [{"N": N, "K": K, "floor_us": round(f * 1e6, 3), "floor_gbs": round(N * K / f / 1e9, 1),
+                  "gemm_us": round(g * 1e6, 3), "gemm_over_floor": round(g / f, 3)}
+                 for (N, K), f, g in zip(wl.shapes, fts, gemm_ts)]
     # the activation quantisation, reported on its own (HBM bound at large M)
     act_quant = None
     if not wl.bf16_in and not wl.grouped:
@@ -713,11 +741,16 @@ def main() -> None:
                    "graphs": f"{S} steps per CUDA graph replay ({launches_per_step} kernels per step)",
                    "steps_per_graph": S,
                    "parallelism": f"replicas x{world}"},
+        "repeats": {"n": len(rep_ms), "ms_per_step_min": round(min(rep_ms), 5) if rep_ms else None,
+                    "ms_per_step_median": round(statistics.median(rep_ms), 5) if rep_ms else None,
+                    "ms_per_step_max": round(max(rep_ms), 5) if rep_ms else None},
         "us_per_call": per_shape,
         "act_quant": act_quant,
+        "floor": floor,
         "gpu_launches": args.steps * launches_per_step,
         "roofline": {"bound": bound, "kernel": kernel, "achieved": round(achieved, 1),
                      "peak": round(peak, 1), "unit": roof_unit, "frac": round(achieved / peak, 4),
+                     "frac_nominal": round(achieved / (NOMINAL_HBM_GBS if bound == "hbm" else NOMINAL_FP8_TFLOPS), 4),
                      "traffic": traffic, "peak_kind": peak_kind, **per_launch,
                      "us_per_launch": round(sum(gemm_ts) / len(gemm_ts) * 1e6, 3)},
         "e2e": {"value": round(world * (step_flops / 1e12 if bound == "tensor" else step_bytes / 1e9) / t_e2e, 2),
@@ -735,7 +768,11 @@ def main() -> None:
     if not args.no_sweep and rank == 0 and args.workload == "decode":
         del wl
         torch.cuda.empty_cache()
-        result["sweep"] = sweep(weights, device, stream, peaks)
+        sw_res = sweep(weights, device, stream, peaks)
+        # ahead of the long fields, so that a truncated tail of the line keeps it
+        keys = list(result)
+        at = keys.index("us_per_call")
+        result = {**{k: result[k] for k in keys[:at]}, "sweep": sw_res, **{k: result[k] for k in keys[at:]}}
     if rank == 0 and not args.no_cpu_baseline:
         cb = oracle_step_time(budget_s=args.cpu_budget)
         result["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "single_thread_value")}

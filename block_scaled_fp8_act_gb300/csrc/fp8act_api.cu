@@ -282,13 +282,25 @@ int fp8act_check_status(void* stream) {
     }
     const unsigned int tc = fp8act::read_and_clear_tc_error();
     const unsigned int mid = fp8act::read_and_clear_midm_error();
-    return (tc | mid) ? FP8ACT_ERR_TIMEOUT : FP8ACT_OK;
+    const unsigned int rd = fp8act::read_and_clear_read_error();
+    return (tc | mid | rd) ? FP8ACT_ERR_TIMEOUT : FP8ACT_OK;
 }
 
 int fp8act_set_wait_limit(long long limit_ns, int withhold_first_load) {
     g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
     g_withhold_first_load.store(withhold_first_load ? 1 : 0, std::memory_order_relaxed);
     return FP8ACT_OK;
+}
+
+int fp8act_stream_read(const void* src, size_t bytes, unsigned int* sink, void* stream) {
+    if (bytes == 0) return FP8ACT_OK;
+    if (!src || !sink) return FP8ACT_ERR_NULL;
+    if (!aligned(src, 16) || !aligned(sink, 4) || bytes % 16) return FP8ACT_ERR_ALIGN;
+    int st = FP8ACT_OK;
+    const int sms = current_device_sms(&st);
+    if (st) return st;
+    return launch_status(fp8act::launch_stream_read(src, static_cast<int64_t>(bytes), sink, sms,
+                                                    static_cast<cudaStream_t>(stream)));
 }
 
 int fp8act_version(void) { return 200; }

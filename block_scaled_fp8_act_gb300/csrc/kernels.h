@@ -80,10 +80,16 @@ constexpr int kMidMaxTokens = 128;  // the kernel itself handles up to 128
 cudaError_t launch_gemm_midm(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N,
                              int K, void* out, bool out_f32, int num_sms, cudaStream_t stream);
 
+// Diagnostic streaming read of `bytes` (a multiple of 16) from `src`: one CTA
+// per SM, a ring of TMA bulk copies, launched like the GEMMs; folds the data
+// into *sink.
+cudaError_t launch_stream_read(const void* src, int64_t bytes, unsigned int* sink, int num_sms, cudaStream_t stream);
+
 // Device-side error words of the tcgen05 kernels (non-zero after a bounded
 // wait gave up); reading one synchronises with the device and clears it.
 unsigned int read_and_clear_tc_error();
 unsigned int read_and_clear_midm_error();
+unsigned int read_and_clear_read_error();  // the streaming-read diagnostic
 
 // Launch arguments of the tcgen05 kernels' failure path, set process-wide by
 // the fp8act_set_wait_limit() test hook: the wall-time bound of every wait

@@ -64,11 +64,12 @@ def load(build: bool = False) -> ctypes.CDLL:
     L.fp8act_strerror.restype = ctypes.c_char_p
     L.fp8act_check_status.argtypes = [p]
     L.fp8act_set_wait_limit.argtypes = [ctypes.c_longlong, i]
+    L.fp8act_stream_read.argtypes = [p, ctypes.c_size_t, p, p]
     for fn in (L.fp8_act_quant, L.fp8_weight_quant, L.fp8_block_gemm, L.fp8_block_gemm_f32,
                L.fp8_block_gemm_w8a16, L.fp8_block_gemm_w8a16_f32,
                L.fp8_act_quant_grouped, L.fp8_block_gemm_grouped, L.fp8_block_gemm_grouped_f32,
                L.fp8_linear, L.fp8_linear_f32,
-               L.fp8act_check_status, L.fp8act_set_wait_limit, L.fp8act_version):
+               L.fp8act_check_status, L.fp8act_set_wait_limit, L.fp8act_version, L.fp8act_stream_read):
         fn.restype = ctypes.c_int
     _lib = L
     return L
@@ -280,3 +281,12 @@ def set_wait_limit(limit_ns: int, withhold_first_load: bool = False) -> None:
     the wall-time bound of their waits (negative = the 2 s default) and whether
     each CTA skips its first operand copy."""
     _check("fp8act_set_wait_limit", load().fp8act_set_wait_limit(int(limit_ns), 1 if withhold_first_load else 0))
+
+
+def stream_read(src: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """Diagnostic: read every byte of the CUDA tensor `src` once (the weight-stream
+    floor), folding it into the int32 CUDA tensor `sink` (see fp8act_stream_read)."""
+    if not src.is_cuda or not src.is_contiguous() or not sink.is_cuda or sink.dtype != torch.int32:
+        raise TypeError("src must be a contiguous CUDA tensor and sink an int32 CUDA tensor")
+    _check("fp8act_stream_read", load().fp8act_stream_read(src.data_ptr(), src.numel() * src.element_size(),
+                                                           sink.data_ptr(), _stream(stream)))

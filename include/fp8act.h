@@ -46,6 +46,8 @@
 #define FP8ACT_API
 #endif
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -240,6 +242,24 @@ FP8ACT_API int fp8act_check_status(void* stream);
  * keeps the values it was captured with). Always returns FP8ACT_OK.
  */
 FP8ACT_API int fp8act_set_wait_limit(long long limit_ns, int withhold_first_load);
+
+/*
+ * Diagnostic: the floor of a weight stream. Reads `bytes` bytes of device
+ * memory at `src` once, one CTA per SM streaming a contiguous share through a
+ * ring of 32 KB TMA bulk copies, launched exactly like the GEMMs above
+ * (programmatic dependent launch: the reads start before the previous kernel
+ * on the stream has finished), and XORs a fold of the data into *sink. Its
+ * waits are bounded like the tcgen05 kernels' (fp8act_check_status). A chain of these calls over buffers the size
+ * of a layer's weights times the plain streaming read the GEMM's weight
+ * stream is compared against. The section "算子优化" of the smartx.com
+ * Qwen3.8-27B post puts the decode step's weight-reading GEMMs "near the
+ * bandwidth lower bound"; this call measures that bound on the device.
+ *   src   16-byte aligned device pointer; bytes a multiple of 16
+ *   sink  4-byte aligned device word (read-modify-written)
+ * Errors: FP8ACT_ERR_NULL, FP8ACT_ERR_ALIGN (also for bytes % 16 != 0),
+ * FP8ACT_ERR_DEVICE, FP8ACT_ERR_LAUNCH.
+ */
+FP8ACT_API int fp8act_stream_read(const void* src, size_t bytes, unsigned int* sink, void* stream);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 FP8ACT_API int fp8act_version(void);

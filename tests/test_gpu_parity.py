@@ -585,3 +585,15 @@ def test_act_quant_bit_exact_over_many_scales(fp8act):
     assert np.array_equal(sa.cpu().numpy(), sa_ref)
     assert np.array_equal(q.cpu().numpy(), q_ref)
 
+
+
+def test_stream_read_folds_every_word(fp8act):
+    """The weight-stream floor diagnostic reads every 32-bit word of the
+    buffer exactly once: the folded result is the XOR of all of them."""
+    g = torch.Generator(device="cpu").manual_seed(5)
+    src = torch.randint(0, 256, (3 * 1024 * 1024 + 48,), dtype=torch.uint8, generator=g)
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fp8act.stream_read(src.cuda(), sink)
+    torch.cuda.synchronize()
+    want = np.bitwise_xor.reduce(src.numpy().view(np.uint32))
+    assert int(sink.cpu().numpy().view(np.uint32)[0]) == int(want)
