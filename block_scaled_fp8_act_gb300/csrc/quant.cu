@@ -1,13 +1,20 @@
 // Activation (1x128) and weight (128x128) quantisation to E4M3 with fp32 scales.
 //
 // Both follow one rule per group: s = amax / 448 (IEEE fp32 division),
-// s = 1 for an all-zero group, code = E4M3(x / s) with an IEEE fp32 division
-// per element and a round-to-nearest-even, saturating conversion. The
-// division is kept (not a multiply by 1/s) because the two differ in the last
-// bit often enough to change codes. This is the "W8A8 Block FP8" layer of the
-// dual-L20 Qwen3.8-27B-FP8 tuning report (section 8); the pages do not spell
-// out the arithmetic, and the rule above is the plain reading of an amax/448
-// fp32 scale.
+// s = 1 for an all-zero group, code = E4M3(x / s), the IEEE fp32 quotient
+// rounded to nearest even, saturating. This is the "W8A8 Block FP8" layer of
+// the dual-L20 Qwen3.8-27B-FP8 tuning report (section 8); the pages do not
+// spell out the arithmetic, and the rule above is the plain reading of an
+// amax/448 fp32 scale. A plain multiply by 1/s is not enough: it changes a
+// code whenever the quotient sits within an ulp or two of an E4M3 rounding
+// midpoint, which bf16 inputs hit often (their short significands make many
+// quotients exact midpoints). The activation path forms the scale, the
+// reciprocal and the quotients from short fused multiply-add sequences that
+// give the IEEE results' scales and codes for every input (act_group.cuh
+// says how that was established); the offline weight path keeps the plain
+// IEEE division.
+#include <atomic>
+
 #include "act_group.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -21,7 +28,18 @@ namespace {
 // lanes with xor shuffles, and each lane stores its 8 codes (8 bytes).
 // Groups are contiguous in memory because K % 128 == 0, so group g of the
 // flattened [M*K/128] index starts at element 128 g and its scale is sa[g].
+// A warp takes 2 * kActUnroll groups per iteration and issues the loads of
+// its next iteration before quantising the current one, so every warp keeps
+// two iterations of loads in flight. At large M the kernel is bound by the
+// instruction issue and the latency of each group's chain (loads, shuffles,
+// scale, reciprocal, quotients); measured at M = 4096, K = 5120 / 8704:
+// 5 CTAs of 256 threads per SM (the launch bound below) with two groups per
+// half-warp and a grid of exactly the resident CTAs beat deeper unrolls,
+// 4, 6 or 8 CTAs per SM (8 spill, and a grid of 8 per SM with 5 resident
+// runs in 1.6 waves) and a TMA bulk-copy ring feeding shared memory.
 constexpr int kActUnroll = 2;
+constexpr int kActThreads = 256;
+constexpr int kActMinCtas = 5;
 constexpr int kMaxActProblems = 16;
 
 // Where group g of the flattened index lives: one problem ...
@@ -68,44 +86,54 @@ __device__ __forceinline__ void act_quant_body(const Map& map, int64_t groups) {
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t per_iter = 2 * kActUnroll;  // groups one warp handles per iteration
+    const int64_t step = nwarp * per_iter;
+    auto load = [&](int64_t base, uint4 (&v)[kActUnroll]) {
+#pragma unroll
+        for (int u = 0; u < kActUnroll; ++u) {
+            const int64_t g = base + 2 * u + half;
+            const uint4* xg = nullptr;
+            uint2* qg;
+            float* sg;
+            if (g < groups) map.at(g, xg, qg, sg);
+            v[u] = g < groups ? ld_dep_stream_v4(xg + hl) : make_uint4(0, 0, 0, 0);
+        }
+    };
 
     // Programmatic dependent launch: let the next kernel (the GEMM, whose
     // weight stream does not depend on us) start launching now, then wait for
     // the grid that produced x (and may still read q / sa) to finish.
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
-    for (int64_t base = warp * per_iter; base < groups; base += nwarp * per_iter) {
-        uint4 v[kActUnroll];
-        uint2* qg[kActUnroll];
-        float* sg[kActUnroll];
-#pragma unroll
-        for (int u = 0; u < kActUnroll; ++u) {
-            const int64_t g = base + 2 * u + half;
-            const uint4* xg = nullptr;
-            qg[u] = nullptr;
-            sg[u] = nullptr;
-            if (g < groups) map.at(g, xg, qg[u], sg[u]);
-            v[u] = g < groups ? ld_dep_stream_v4(xg + hl) : make_uint4(0, 0, 0, 0);
-        }
+    uint4 v[kActUnroll];
+    load(warp * per_iter, v);
+    for (int64_t base = warp * per_iter; base < groups; base += step) {
+        uint4 next[kActUnroll];
+        load(base + step, next);
 #pragma unroll
         for (int u = 0; u < kActUnroll; ++u) {
             const int64_t g = base + 2 * u + half;
             uint2 codes;
             const float s = quant_group_halfwarp(v[u], codes);
             if (g < groups) {
-                qg[u][hl] = codes;
-                if (hl == 0) *sg[u] = s;
+                const uint4* xg;
+                uint2* qg;
+                float* sg;
+                map.at(g, xg, qg, sg);
+                qg[hl] = codes;
+                if (hl == 0) *sg = s;
             }
         }
+#pragma unroll
+        for (int u = 0; u < kActUnroll; ++u) v[u] = next[u];
     }
 }
 
-__global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict__ x, int64_t groups,
+__global__ void __launch_bounds__(kActThreads, kActMinCtas) act_quant_kernel(const uint4* __restrict__ x, int64_t groups,
                                                         uint2* __restrict__ q, float* __restrict__ sa) {
     act_quant_body(ActSingle{x, q, sa}, groups);
 }
 
-__global__ void __launch_bounds__(256) act_quant_grouped_kernel(const __grid_constant__ ActGroupedArgs a) {
+__global__ void __launch_bounds__(kActThreads, kActMinCtas) act_quant_grouped_kernel(const __grid_constant__ ActGroupedArgs a) {
     act_quant_body(ActGrouped{&a}, a.groups);
 }
 
@@ -154,22 +182,36 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t* __res
 
 }  // namespace
 
-static cudaError_t act_quant_config(int64_t groups, int num_sms, cudaStream_t stream, cudaLaunchConfig_t& cfg,
+// Resident CTAs per SM of an activation kernel (occupancy API, cached per
+// device); the grid never exceeds one wave of them.
+static int act_ctas_per_sm(const void* kernel, std::atomic<int> (&cache)[64]) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int v = cache[dev & 63].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, kActThreads, 0) != cudaSuccess || v < 1) {
+            cudaGetLastError();
+            v = kActMinCtas;
+        }
+        cache[dev & 63].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+static void act_quant_config(int64_t groups, int num_sms, int per_sm, cudaStream_t stream, cudaLaunchConfig_t& cfg,
                              cudaLaunchAttribute (&attr)[1]) {
-    const int threads = 256;
-    const int64_t groups_per_block = (threads / 32) * 2 * kActUnroll;
+    const int64_t groups_per_block = (kActThreads / 32) * 2 * kActUnroll;
     int64_t blocks = (groups + groups_per_block - 1) / groups_per_block;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
     if (blocks > cap) blocks = cap;
     cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-    cfg.blockDim = dim3(threads);
+    cfg.blockDim = dim3(kActThreads);
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaSuccess;
 }
 
 cudaError_t launch_act_quant_grouped(const ActQuantProblem* probs, int count, int num_sms, cudaStream_t stream) {
@@ -187,18 +229,22 @@ cudaError_t launch_act_quant_grouped(const ActQuantProblem* probs, int count, in
     a.count = count;
     a.groups = groups;
     if (groups == 0) return cudaSuccess;
+    static std::atomic<int> per_sm[64];
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    act_quant_config(groups, num_sms, stream, cfg, attr);
+    act_quant_config(groups, num_sms, act_ctas_per_sm(reinterpret_cast<const void*>(act_quant_grouped_kernel), per_sm),
+                     stream, cfg, attr);
     return cudaLaunchKernelEx(&cfg, act_quant_grouped_kernel, a);
 }
 
 cudaError_t launch_act_quant(const void* x, int64_t M, int64_t K, void* q, float* sa, int num_sms,
                              cudaStream_t stream) {
     const int64_t groups = M * (K / kGroup);
+    static std::atomic<int> per_sm[64];
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    act_quant_config(groups, num_sms, stream, cfg, attr);
+    act_quant_config(groups, num_sms, act_ctas_per_sm(reinterpret_cast<const void*>(act_quant_kernel), per_sm), stream,
+                     cfg, attr);
     return cudaLaunchKernelEx(&cfg, act_quant_kernel, static_cast<const uint4*>(x), groups,
                               static_cast<uint2*>(q), sa);
 }

@@ -586,6 +586,43 @@ def test_act_quant_bit_exact_over_many_scales(fp8act):
     assert np.array_equal(q.cpu().numpy(), q_ref)
 
 
+def _division_domain_groups(ab_lo: int, ab_hi: int) -> np.ndarray:
+    """bf16 bit patterns [groups, 128]: for every positive amax pattern ab in
+    [ab_lo, ab_hi], groups whose element 0 is amax and whose other 127
+    elements run through every bf16 x with |x| <= amax, both signs (zero
+    padded), so each group's amax is exactly ab."""
+    blocks = []
+    for ab in range(ab_lo, ab_hi + 1):
+        mags = np.arange(ab + 1, dtype=np.uint16)
+        xs = np.concatenate([mags, mags | np.uint16(0x8000)])
+        g = -(-xs.size // 127)
+        flat = np.zeros(g * 127, np.uint16)
+        flat[:xs.size] = xs
+        block = np.empty((g, 128), np.uint16)
+        block[:, 0] = ab
+        block[:, 1:] = flat.reshape(g, 127)
+        blocks.append(block)
+    return np.concatenate(blocks)
+
+
+def test_act_quant_bit_exact_over_whole_quotient_domain(fp8act):
+    """Every pair (group amax, element x) of bf16 values with |x| <= amax for
+    amax from just below 2^-70 to just above 2^70 (~590M values, the range
+    where the kernel forms x / s from the reciprocal of s plus one residual
+    correction, and a few patterns on each side where it divides): codes and
+    scales equal the oracle's IEEE-division quantisation."""
+    lo, hi = 0x1C70, 0x6290  # bf16 patterns of 2^-70 - 16 ulps .. 2^70 + 16 ulps
+    step = 1024
+    for a0 in range(lo, hi + 1, step):
+        bits = _division_domain_groups(a0, min(a0 + step - 1, hi))
+        xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+        q, sa = fp8act.fp8_act_quant(xb.cuda())
+        torch.cuda.synchronize()
+        q_ref, sa_ref = oracle.act_quant(bits)
+        assert np.array_equal(sa.cpu().numpy(), sa_ref), hex(a0)
+        bad = np.nonzero(q.cpu().numpy() != q_ref)
+        assert bad[0].size == 0, (hex(a0), bits[bad[0][0]].tolist()[:4], bad[1][:4])
+
 
 def test_stream_read_folds_every_word(fp8act):
     """The weight-stream floor diagnostic reads every 32-bit word of the
