@@ -118,8 +118,8 @@ def load_peaks() -> tuple[dict, str]:
 
 
 KERNEL_SOURCES = {
-    "gemm_skinny_kernel": ("gemm_skinny.cu", "common.cuh", "sm100_ptx.cuh"),
-    "gemm_skinny_grouped_kernel": ("gemm_skinny.cu", "common.cuh", "sm100_ptx.cuh"),
+    "gemm_skinny_kernel": ("gemm_skinny.cu", "act_group.cuh", "common.cuh", "sm100_ptx.cuh"),
+    "gemm_skinny_grouped_kernel": ("gemm_skinny.cu", "act_group.cuh", "common.cuh", "sm100_ptx.cuh"),
     "gemm_tc_kernel": ("gemm_tc.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
     "gemm_midm_kernel": ("gemm_midm.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
 }
