@@ -524,6 +524,248 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
     return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel<kF32Out, kUnroll, kTG, kMode>, q, sa, w, sw, M, N, K, out);
 }
 
+// ------------------------------------------------------------------------
+// Fused mode with one quantisation per SM (M <= 8). One CTA per SM, up to 32
+// warps in groups of `wg`; each group takes the weight tiles
+// blockIdx.x * groups + group, + gridDim.x * groups, ... and runs the
+// two-launch kernel's loop on each (the same warp count per tile, so the
+// same K order and sums), reading the activation codes and scales from
+// shared memory, where the CTA's warps put them once, after the
+// programmatic-launch wait, with the activation kernel's group code. The
+// first weight steps of every group's first tile go to L2 before the wait.
+constexpr int kPqMaxWarps = 32;
+constexpr int kPqMaxGroups = 15;  // named barriers 1..15 (0 is __syncthreads)
+// activation groups per half-warp slot and quantisation pass: 4 where the
+// prologue holds no weight registers (depth 1), 2 where it does (depth 4)
+template <int kUnroll>
+constexpr int pq_quant_unroll() { return kUnroll > 1 ? 2 : 4; }
+template <int kUnroll>
+constexpr int pq_max_warps() { return kUnroll == 1 ? kPqMaxWarps : kPqMaxWarps / 2; }  // 64 / 128 registers
+
+struct PqArgs {
+    const uint8_t* x;  // bf16 activations [M][K]
+    const uint8_t* w;
+    const float* sw;
+    void* out;
+    int M, N, K, KB, tiles;
+    int wg;      // warps per tile
+    int groups;  // warp groups per CTA
+};
+
+__host__ __device__ inline int pq_codes_stride(int K) { return K + 16; }  // padded rows
+__host__ __device__ inline int pq_sa_offset(int M, int K) { return (M * pq_codes_stride(K) + 15) & ~15; }
+__host__ __device__ inline int pq_red_offset(int M, int K, int KB) { return pq_sa_offset(M, K) + ((M * KB * 4 + 15) & ~15); }
+inline size_t pq_smem_bytes(int M, int K, int groups, int wg) {
+    return static_cast<size_t>(pq_red_offset(M, K, K / kGroup)) + static_cast<size_t>(groups) * wg * 16 * 8 * 4;
+}
+
+// One 16-row tile by the warps of one group: the W8A8 loop of skinny_tile
+// (same load depth, K permutation, MMA order, scale products and warp-order
+// sum), with the codes and scales read from shared memory.
+template <bool kF32Out, int kUnroll, bool kWide, class Prologue>
+__device__ __forceinline__ void pq_tile(const PqArgs& a, const uint8_t* __restrict__ q_s, const float* __restrict__ sa_s,
+                                        float (*red)[16][8], int tile, int gw, uint32_t bar_id, bool run_prologue,
+                                        const Prologue& prologue) {
+    const int KB = a.KB, K = a.K, M = a.M, N = a.N, wg = a.wg;
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int n0 = tile * 16;
+    const bool ok_r0 = n0 + g < N, ok_r1 = n0 + g + 8 < N;
+    const int lane_off = kWide ? 32 * t : 16 * t;
+    constexpr int kHiOff = kWide ? 16 : 64;
+    const uint8_t* w_r0 = a.w + static_cast<int64_t>(n0 + g) * K + lane_off;
+    const uint8_t* w_r1 = a.w + static_cast<int64_t>(n0 + g + 8) * K + lane_off;
+    const float* sw_r = a.sw + static_cast<int64_t>(n0 / kGroup) * KB;
+    const int stride = wg * kUnroll;
+    const bool pf_lane = lane < 16 && n0 + lane < N;
+    const uint8_t* w_pf = a.w + static_cast<int64_t>(n0 + lane) * K;
+    if (pf_lane) {
+#pragma unroll
+        for (int s = 1; s <= kL2Ahead; ++s)
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int kb = gw + s * stride + u * wg;
+                if (kb < KB) prefetch_l2(w_pf + static_cast<int64_t>(kb) * kGroup);
+            }
+    }
+    const bool ok_x = g < M;
+    const uint8_t* x_r = q_s + g * pq_codes_stride(K) + lane_off;
+    const int c0 = 2 * t;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kb0 = gw; kb0 < KB; kb0 += stride) {
+        if (pf_lane) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int kb = kb0 + (kL2Ahead + 1) * stride + u * wg;
+                if (kb < KB) prefetch_l2(w_pf + static_cast<int64_t>(kb) * kGroup);
+            }
+        }
+        uint4 r0lo[kUnroll], r0hi[kUnroll], r1lo[kUnroll], r1hi[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int kb = kb0 + u * wg;
+            const bool ok_k = kb < KB;
+            const int64_t off = static_cast<int64_t>(kb) * kGroup;
+            if constexpr (kWide) {
+                r0lo[u] = r0hi[u] = r1lo[u] = r1hi[u] = zero;
+                if (ok_k && ok_r0) ld_stream_v8(w_r0 + off, r0lo[u], r0hi[u]);
+                if (ok_k && ok_r1) ld_stream_v8(w_r1 + off, r1lo[u], r1hi[u]);
+            } else {
+                r0lo[u] = (ok_k && ok_r0) ? ld_stream_v4(w_r0 + off) : zero;
+                r0hi[u] = (ok_k && ok_r0) ? ld_stream_v4(w_r0 + off + 64) : zero;
+                r1lo[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off) : zero;
+                r1hi[u] = (ok_k && ok_r1) ? ld_stream_v4(w_r1 + off + 64) : zero;
+            }
+        }
+        if (run_prologue) {  // the first tile: its first weight loads are in flight
+            prologue();
+            run_prologue = false;
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int kb = kb0 + u * wg;
+            if (kb < KB) {
+                const uint4 xlo = ok_x ? *reinterpret_cast<const uint4*>(x_r + kb * kGroup) : zero;
+                const uint4 xhi = ok_x ? *reinterpret_cast<const uint4*>(x_r + kb * kGroup + kHiOff) : zero;
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_e4m3_16x8x32(d, r0lo[u].x, r1lo[u].x, r0lo[u].y, r1lo[u].y, xlo.x, xlo.y);
+                mma_e4m3_16x8x32(d, r0lo[u].z, r1lo[u].z, r0lo[u].w, r1lo[u].w, xlo.z, xlo.w);
+                mma_e4m3_16x8x32(d, r0hi[u].x, r1hi[u].x, r0hi[u].y, r1hi[u].y, xhi.x, xhi.y);
+                mma_e4m3_16x8x32(d, r0hi[u].z, r1hi[u].z, r0hi[u].w, r1hi[u].w, xhi.z, xhi.w);
+                const float s_w = __ldg(sw_r + kb);
+                const float sa0 = c0 < M ? sa_s[c0 * KB + kb] : 0.f;
+                const float sa1 = c0 + 1 < M ? sa_s[(c0 + 1) * KB + kb] : 0.f;
+                const float s0 = sa0 * s_w;
+                const float s1 = sa1 * s_w;
+                acc[0] = fmaf(d[0], s0, acc[0]);
+                acc[1] = fmaf(d[1], s1, acc[1]);
+                acc[2] = fmaf(d[2], s0, acc[2]);
+                acc[3] = fmaf(d[3], s1, acc[3]);
+            }
+        }
+    }
+    red[gw][g][2 * t] = acc[0];
+    red[gw][g][2 * t + 1] = acc[1];
+    red[gw][g + 8][2 * t] = acc[2];
+    red[gw][g + 8][2 * t + 1] = acc[3];
+    ptx::named_bar_sync(bar_id, wg * 32);
+    for (int i = gw * 32 + lane; i < 16 * 8; i += wg * 32) {
+        const int r = i & 15, c = i >> 4;
+        float v = 0.f;
+        for (int ww = 0; ww < wg; ++ww) v += red[ww][r][c];
+        const int n = n0 + r;
+        if (n < N && c < M) {
+            const int64_t o = static_cast<int64_t>(c) * N + n;
+            if constexpr (kF32Out)
+                static_cast<float*>(a.out)[o] = v;
+            else
+                static_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(v);
+        }
+    }
+    ptx::named_bar_sync(bar_id, wg * 32);  // the partial sums are read before the next tile writes them
+}
+
+template <bool kF32Out, int kUnroll, bool kWide>
+__global__ void __launch_bounds__(pq_max_warps<kUnroll>() * 32, 1) linear_persistent_kernel(const __grid_constant__ PqArgs a) {
+    extern __shared__ __align__(16) uint8_t pq_smem[];
+    uint8_t* const q_s = pq_smem;
+    float* const sa_s = reinterpret_cast<float*>(pq_smem + pq_sa_offset(a.M, a.K));
+    float(*const red_all)[16][8] = reinterpret_cast<float(*)[16][8]>(pq_smem + pq_red_offset(a.M, a.K, a.KB));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const int group = warp / a.wg, gw = warp % a.wg;
+    const int step = gridDim.x * a.groups;
+
+    ptx::griddep_launch_dependents();
+    // Everything that needs the previous grid's output, run by every thread
+    // exactly once: the wait, the quantisation of every 1x128 group of the M
+    // tokens with the activation kernel's group code, and the CTA barrier
+    // after which the codes are read. Group i goes to half-warp slot
+    // i % (2 nwarps), so every warp shares the work, and a slot's groups of
+    // one pass (pq_quant_unroll) have their loads issued together.
+    auto prologue = [&]() {
+        ptx::griddep_wait();
+        const int half = lane >> 4, hl = lane & 15;
+        const int ngroups = a.M * a.KB;
+        const int slots = 2 * nwarps;
+        const int slot = 2 * warp + half;
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        constexpr int kQU = pq_quant_unroll<kUnroll>();
+        for (int base = 0; base < ngroups; base += kQU * slots) {
+            uint4 v[kQU];
+#pragma unroll
+            for (int u = 0; u < kQU; ++u) {
+                const int gi = base + u * slots + slot;
+                const bool ok = gi < ngroups;
+                const int r = ok ? gi / a.KB : 0, kb = ok ? gi % a.KB : 0;
+                v[u] = ok ? ld_dep_stream_v4(a.x + (static_cast<int64_t>(r) * a.K + kb * kGroup + 8 * hl) * 2) : zero;
+            }
+#pragma unroll
+            for (int u = 0; u < kQU; ++u) {
+                if (base + u * slots + 2 * warp >= ngroups) break;  // warp-uniform: the group code shuffles
+                const int gi = base + u * slots + slot;
+                const bool ok = gi < ngroups;
+                const int r = ok ? gi / a.KB : 0, kb = ok ? gi % a.KB : 0;
+                uint2 codes;
+                const float sg = quant_group_halfwarp(v[u], codes);
+                if (ok) {
+                    *reinterpret_cast<uint2*>(q_s + r * pq_codes_stride(a.K) + kb * kGroup + 8 * hl) = codes;
+                    if (hl == 0) sa_s[r * a.KB + kb] = sg;
+                }
+            }
+        }
+        __syncthreads();
+    };
+    float(*const red)[16][8] = red_all + group * a.wg;
+    const int first = blockIdx.x * a.groups + group;
+    // Depth 4 (short K): the first tile issues its first weight loads (four
+    // K blocks per warp) before the prologue, as the two-launch kernel does
+    // before its wait. Depth 1: the first tile's lines are only prefetched to
+    // L2 before the prologue; holding the loads across it measured slower
+    // there (64 registers: the prologue's own registers crowd them).
+    constexpr bool kLoadsFirst = kUnroll > 1;
+    if (!kLoadsFirst || first >= a.tiles) {  // a group without tiles still takes part in the prologue
+        if (!kLoadsFirst && first < a.tiles && lane < 16 && first * 16 + lane < a.N) {
+            const uint8_t* w_pf = a.w + static_cast<int64_t>(first * 16 + lane) * a.K;
+#pragma unroll
+            for (int st = 0; st <= kL2Ahead; ++st) {
+                const int kb = gw + st * a.wg;
+                if (kb < a.KB) prefetch_l2(w_pf + static_cast<int64_t>(kb) * kGroup);
+            }
+        }
+        prologue();
+        if (first >= a.tiles) return;
+    }
+    pq_tile<kF32Out, kUnroll, kWide>(a, q_s, sa_s, red, first, gw, 1 + group, kLoadsFirst, prologue);
+    for (int tile = first + step; tile < a.tiles; tile += step)
+        pq_tile<kF32Out, kUnroll, kWide>(a, q_s, sa_s, red, tile, gw, 1 + group, false, prologue);
+}
+
+template <bool kF32Out, int kUnroll, bool kWide>
+cudaError_t launch_persistent(const PqArgs& a, int grid, size_t smem, cudaStream_t stream) {
+    static std::atomic<uint64_t> configured{0};  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        const cudaError_t e = cudaFuncSetAttribute(linear_persistent_kernel<kF32Out, kUnroll, kWide>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_release);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(a.groups * a.wg * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, linear_persistent_kernel<kF32Out, kUnroll, kWide>, a);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
@@ -641,8 +883,59 @@ bool fused_fits(int M, int K) {
     return static_cast<size_t>(KB) * (M < 8 ? M : 8) * (kGroup + 4) + 15 * kMaxWarps <= kFqMaxSmem;
 }
 
+namespace {
+
+// The fused kernel with one quantisation per SM, M <= 8; cudaErrorNotSupported
+// (nothing launched) when the codes do not fit shared memory.
+template <bool kF32Out, int kUnroll, bool kWide>
+cudaError_t launch_persistent_typed(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
+                                    int num_sms, cudaStream_t stream) {
+    PqArgs a;
+    a.x = static_cast<const uint8_t*>(x);
+    a.w = w;
+    a.sw = sw;
+    a.out = out;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.KB = K / kGroup;
+    a.tiles = (N + 15) / 16;
+    // warps per tile: the two-launch kernel's choice for this shape (same K order, same sums)
+    constexpr int kMode = kWide ? (kModeW8A8 | kWideBit) : kModeW8A8;
+    int wv = pick_warps<kF32Out, kUnroll, 1, kMode>(a.tiles, a.KB, num_sms, nullptr, M);
+    if (wv == 0) wv = a.KB < 4 ? a.KB : 4;
+    a.wg = wv;
+    int groups = pq_max_warps<kUnroll>() / wv;
+    if (groups > kPqMaxGroups) groups = kPqMaxGroups;
+    const int per_sm = (a.tiles + num_sms - 1) / num_sms;
+    if (groups > per_sm) groups = per_sm;
+    if (groups < 1) return cudaErrorNotSupported;
+    a.groups = groups;
+    const size_t smem = pq_smem_bytes(M, K, groups, wv);
+    if (smem > 227 * 1024) return cudaErrorNotSupported;
+    const int64_t want = (static_cast<int64_t>(a.tiles) + groups - 1) / groups;
+    const int grid = static_cast<int>(want < num_sms ? want : num_sms);
+    return launch_persistent<kF32Out, kUnroll, kWide>(a, grid, smem, stream);
+}
+
+template <bool kF32Out>
+cudaError_t launch_persistent_any(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
+                                  int num_sms, cudaStream_t stream) {
+    if (K / kGroup >= 32) return launch_persistent_typed<kF32Out, 1, false>(x, w, sw, M, N, K, out, num_sms, stream);
+    if ((reinterpret_cast<uintptr_t>(w) & 31) == 0)
+        return launch_persistent_typed<kF32Out, 4, true>(x, w, sw, M, N, K, out, num_sms, stream);
+    return launch_persistent_typed<kF32Out, 4, false>(x, w, sw, M, N, K, out, num_sms, stream);
+}
+
+}  // namespace
+
 cudaError_t launch_linear_fused(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
                                 bool out_f32, int num_sms, cudaStream_t stream) {
+    if (M <= 8) {
+        const cudaError_t e = out_f32 ? launch_persistent_any<true>(x, w, sw, M, N, K, out, num_sms, stream)
+                                      : launch_persistent_any<false>(x, w, sw, M, N, K, out, num_sms, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     // The W8A8 loop with the same load depth rule as launch_gemm_skinny, so
     // that at equal launch geometry the two paths sum in the same order.
     // 256-bit weight loads on the depth-4 path as in launch_gemm_skinny_unroll
