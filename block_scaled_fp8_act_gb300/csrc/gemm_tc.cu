@@ -96,6 +96,7 @@ struct TcArgs {
     const float* sw;
     void* out;
     int M, N, K, KB, NB;
+    int ldo;  // output row stride (elements): N, or the full width when `out` is a column slice
     unsigned long long wait_ns;  // bound of every wait that can give up (test hook shortens it)
     int withhold;                // test hook: the producer never issues the CTA's first K group
 };
@@ -345,8 +346,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                 // store this thread's row segment directly
                 const int nstart = n0 + hf * C::kCols;
                 if constexpr (kF32Out) {
-                    float* dst = static_cast<float*>(a.out) + static_cast<int64_t>(m) * a.N + nstart;
-                    if ((a.N & 3) == 0 && nstart + C::kCols <= a.N) {
+                    float* dst = static_cast<float*>(a.out) + static_cast<int64_t>(m) * a.ldo + nstart;
+                    if ((a.ldo & 3) == 0 && nstart + C::kCols <= a.N) {
 #pragma unroll
                         for (int j = 0; j < C::kCols; j += 4)
                             *reinterpret_cast<float4*>(dst + j) =
@@ -357,8 +358,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                             if (nstart + j < a.N) dst[j] = acc[j];
                     }
                 } else {
-                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + static_cast<int64_t>(m) * a.N + nstart;
-                    if ((a.N & 7) == 0 && nstart + C::kCols <= a.N) {
+                    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + static_cast<int64_t>(m) * a.ldo + nstart;
+                    if ((a.ldo & 7) == 0 && nstart + C::kCols <= a.N) {
 #pragma unroll
                         for (int j = 0; j < C::kCols; j += 8) {
                             uint4 v;
@@ -420,8 +421,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
                     }
                 const int m = m0 + r, n = n0 + col;
                 if (ok && m < a.M) {
-                    const int64_t o = static_cast<int64_t>(m) * a.N + n;
-                    if (n + 3 < a.N && (a.N & 3) == 0) {
+                    const int64_t o = static_cast<int64_t>(m) * a.ldo + n;
+                    if (n + 3 < a.N && (a.ldo & 3) == 0) {
                         if constexpr (kF32Out) {
                             *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) = v;
                         } else {
@@ -552,6 +553,7 @@ cudaError_t launch_gemm_tc(const uint8_t* q, const float* sa, const uint8_t* w, 
     a.K = K;
     a.KB = K / kGroup;
     a.NB = (N + kGroup - 1) / kGroup;
+    a.ldo = N;
     a.wait_ns = tile_wait_limit_ns();
     a.withhold = tile_withhold_first_load() ? 1 : 0;
     // 256-wide weight tiles when the grid is large (prefill: fewer operand
@@ -559,18 +561,47 @@ cudaError_t launch_gemm_tc(const uint8_t* q, const float* sa, const uint8_t* w, 
     // a batched-decode weight stream over the SMs).
     const int mt = (M + BM - 1) / BM;
     const bool wide = static_cast<int64_t>(mt) * ((N + 255) / 256) >= 2 * num_sms;
-    const int bn = wide ? 256 : 128;
-    CUtensorMap ta, tb;
+    CUtensorMap ta;
     if (!encode_tmap_2d_u8(&ta, q, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K),
-                           kGroup, BM, true) ||
-        !encode_tmap_2d_u8(&tb, w, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K),
-                           kGroup, bn, true))
+                           kGroup, BM, true))
         return cudaErrorInvalidValue;
-    if (wide)
-        return out_f32 ? launch_typed<256, true>(ta, tb, a, num_sms, stream)
-                       : launch_typed<256, false>(ta, tb, a, num_sms, stream);
-    return out_f32 ? launch_typed<128, true>(ta, tb, a, num_sms, stream)
-                   : launch_typed<128, false>(ta, tb, a, num_sms, stream);
+    // One launch over the output columns [n_begin, n_begin + cols) of `out`.
+    auto launch_cols = [&](int bn, int n_begin, int cols) -> cudaError_t {
+        TcArgs s = a;
+        s.N = cols;
+        s.NB = (cols + kGroup - 1) / kGroup;
+        s.sw = sw + static_cast<int64_t>(n_begin / kGroup) * a.KB;
+        s.out = out_f32 ? static_cast<void*>(static_cast<float*>(out) + n_begin)
+                        : static_cast<void*>(static_cast<__nv_bfloat16*>(out) + n_begin);
+        CUtensorMap tb;
+        if (!encode_tmap_2d_u8(&tb, w + static_cast<int64_t>(n_begin) * K, static_cast<uint64_t>(K),
+                               static_cast<uint64_t>(cols), static_cast<uint64_t>(K), kGroup, bn, true))
+            return cudaErrorInvalidValue;
+        if (bn == 256)
+            return out_f32 ? launch_typed<256, true>(ta, tb, s, num_sms, stream)
+                           : launch_typed<256, false>(ta, tb, s, num_sms, stream);
+        return out_f32 ? launch_typed<128, true>(ta, tb, s, num_sms, stream)
+                       : launch_typed<128, false>(ta, tb, s, num_sms, stream);
+    };
+    if (!wide) return launch_cols(128, 0, N);
+    // Split tail wave: the persistent 256-wide launch takes the whole column
+    // groups that fit in its whole waves; the rest (at most half a wave of
+    // 128-wide tiles) runs as a second launch of 128-wide tiles, which splits
+    // K over a cluster of CTAs (the tiles leave SMs idle). Both launches write
+    // column slices of the same output. On the N = 5120 prefill shapes (640
+    // tiles = 4.2 waves) this replaces a fifth wave run by 32 of the 152 CTAs.
+    const int tiles = mt * ((N + 255) / 256);
+    const int waves = tiles / num_sms;
+    const int n_split = (waves * num_sms / mt) * 256;
+    const int tail_tiles = mt * ((N - n_split + 127) / 128);
+    // only where the tail launch can split K at least two ways (measured: an
+    // unsplit 128-wide tail launch did not beat the persistent kernel's own tail)
+    if (waves >= 1 && n_split > 0 && n_split < N && 2 * tail_tiles <= num_sms && a.KB >= 4) {
+        const cudaError_t e = launch_cols(256, 0, n_split);
+        if (e != cudaSuccess) return e;
+        return launch_cols(128, n_split, N - n_split);
+    }
+    return launch_cols(256, 0, N);
 }
 
 }  // namespace fp8act
