@@ -111,17 +111,23 @@ def test_gemm_prefill_sampled_rows(fp8act, si):
 def test_gemm_prefill_ragged_n(fp8act, N, K):
     """M = 4096 with N past the last full 256-wide tile: the last tile's rows
     beyond N read as zero, its scale blocks end inside the tile, and nothing
-    is stored past N."""
+    is stored past N. N = 5000 takes the split tail (a 136-column ragged tail
+    of 128-wide tiles, K split over a cluster)."""
     from parity_util import Problem, tile_rows
     rows = tile_rows(4096, 256, seed=N)
     Problem(N, K, seed=N + K).run_and_compare(4096, seed=7, rows=rows)
 
 
-def test_gemm_prefill_ragged_n_writes_nothing_outside_out(fp8act):
-    """The persistent 256-wide store path with N = 2600 (the last tile ends
-    40 rows past N): canaries on both sides of the output stay intact."""
+@pytest.mark.parametrize("N", [2600, 5064])
+def test_gemm_prefill_ragged_n_writes_nothing_outside_out(fp8act, N):
+    """M = 4096 with a ragged N: 2600 goes through the persistent 256-wide
+    store path alone (the last tile ends 40 rows past N); 5064 through the
+    split tail (19 column groups of 256 in the persistent launch, the last
+    200 columns as 128-wide tiles with K split over a cluster, writing a
+    column slice of the output with the full row stride). Canaries on both
+    sides of the output stay intact."""
     from parity_util import Problem
-    p = Problem(2600, 1024, seed=2600 + 1024)
+    p = Problem(N, 1024, seed=N + 1024)
     M = 4096
     q, sa, _, _ = p.activations(M, seed=5)
     pad = 1 << 16
