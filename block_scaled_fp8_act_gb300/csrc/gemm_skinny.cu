@@ -47,12 +47,18 @@
 // out, in one launch (the quantisation launch per linear layer is what the
 // same post's single-request section credits the weight-only back-end with
 // saving; here the quantisation stays and moves into the GEMM). Each warp
-// quantises, step by step, exactly the 1x128 groups of the K blocks it
-// multiplies (its <= 8 tokens), with the activation kernel's own group code
-// (the same codes and scales bit for bit), into a 1 KB slice of shared memory
-// per block, right after its weight loads for the step are in flight: no
-// warp waits for another and the weight stream never stops. Every CTA
-// repeats the quantisation of the same tokens, so the mode suits small M.
+// quantises exactly the 1x128 groups of the K blocks it multiplies (its <= 8
+// tokens), with the activation kernel's own group code (the same codes and
+// scales bit for bit), into a private slice of shared memory, once its first
+// weight loads are in flight: no warp waits for another. Every CTA repeats
+// the quantisation of the same tokens.
+//
+// Fused, one quantisation per SM (linear_persistent_kernel, M <= 8): one CTA
+// per SM whose warps quantise all the tokens once into shared memory and
+// then, in groups, stream the weight tiles with this file's loop and the
+// two-launch path's warp count per tile (so the same sums); it replaces the
+// per-CTA quantisation, which a timeline trace showed stalling every CTA's
+// weight stream for several microseconds.
 #include <atomic>
 
 #include <cuda_fp16.h>

@@ -55,10 +55,12 @@ struct GemmProblem {
 cudaError_t launch_gemm_skinny_grouped(const GemmProblem* probs, int count, bool out_f32, cudaStream_t stream);
 
 // Fused activation quantisation + block GEMM for small M: bf16 x [M, K] in,
-// out [M, N] as fp8_block_gemm(fp8_act_quant(x)) would give. Each warp
-// quantises the groups of the K blocks it multiplies into its shared-memory
-// slice; fused_fits() tells whether min(8, M) rows of every block fit the
-// kernel's shared-memory ceiling.
+// out [M, N] as fp8_block_gemm(fp8_act_quant(x)) would give. M <= 8: one
+// CTA per SM quantises all the tokens once into shared memory, then warp
+// groups stream the tiles; otherwise (or when the codes do not fit) each
+// warp quantises the groups of the K blocks it multiplies into its
+// shared-memory slice; fused_fits() tells whether min(8, M) rows of every
+// block fit that kernel's shared-memory ceiling.
 bool fused_fits(int M, int K);
 cudaError_t launch_linear_fused(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
                                 bool out_f32, int num_sms, cudaStream_t stream);
