@@ -58,7 +58,11 @@
 // then, in groups, stream the weight tiles with this file's loop and the
 // two-launch path's warp count per tile (so the same sums); it replaces the
 // per-CTA quantisation, which a timeline trace showed stalling every CTA's
-// weight stream for several microseconds.
+// weight stream for several microseconds. From two tokens on, a
+// thread-block cluster of 2 or 4 CTAs shares the quantisation: each CTA
+// quantises every C-th group and stores it into the shared memory of all C
+// CTAs (distributed shared memory), so an SM does 1/C of the work for the
+// price of two cluster barriers.
 #include <atomic>
 
 #include <cuda_fp16.h>
@@ -536,9 +540,10 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
 // blockIdx.x * groups + group, + gridDim.x * groups, ... and runs the
 // two-launch kernel's loop on each (the same warp count per tile, so the
 // same K order and sums), reading the activation codes and scales from
-// shared memory, where the CTA's warps put them once, after the
-// programmatic-launch wait, with the activation kernel's group code. The
-// first weight steps of every group's first tile go to L2 before the wait.
+// shared memory, where the CTA's warps (or, with a cluster, the cluster's
+// CTAs) put them once, after the programmatic-launch wait, with the
+// activation kernel's group code. The first weight steps of every group's
+// first tile go to L2 before the wait.
 constexpr int kPqMaxWarps = 32;
 constexpr int kPqMaxGroups = 15;  // named barriers 1..15 (0 is __syncthreads)
 // activation groups per half-warp slot and quantisation pass: 4 where the
@@ -547,6 +552,22 @@ template <int kUnroll>
 constexpr int pq_quant_unroll() { return kUnroll > 1 ? 2 : 4; }
 template <int kUnroll>
 constexpr int pq_max_warps() { return kUnroll == 1 ? kPqMaxWarps : kPqMaxWarps / 2; }  // 64 / 128 registers
+// CTAs per cluster sharing the quantisation: 1 for one token; otherwise the
+// smallest of 2 and 4 that leaves each SM at most kPqGroupsPerSm of the
+// M x KB activation groups, 4 at most. Measured on the five decode
+// projections at M = 1, 2, 4, 8, alone and in the mixed five-shape step,
+// against every size: an SM quantises ~256 groups per microsecond, a load
+// round trip per pass comes on top, and a cluster costs two cluster barriers
+// and the remote stores (0.5-1.5 us at 4 CTAs); 8 CTAs never beat 4, and at
+// one token (at most ~one group per half-warp) no cluster paid.
+constexpr int kPqGroupsPerSm = 40;
+constexpr int kPqMaxCluster = 4;
+inline int pq_cluster_size(int M, int KB) {
+    if (M <= 1) return 1;
+    int c = 2;
+    while (c < kPqMaxCluster && M * KB > kPqGroupsPerSm * c) c *= 2;
+    return c;
+}
 
 struct PqArgs {
     const uint8_t* x;  // bf16 activations [M][K]
@@ -554,8 +575,9 @@ struct PqArgs {
     const float* sw;
     void* out;
     int M, N, K, KB, tiles;
-    int wg;      // warps per tile
-    int groups;  // warp groups per CTA
+    int wg;       // warps per tile
+    int groups;   // warp groups per CTA
+    int cluster;  // CTAs per thread-block cluster sharing the quantisation (1, 2, 4 or 8)
 };
 
 __host__ __device__ inline int pq_codes_stride(int K) { return K + 16; }  // padded rows
@@ -683,44 +705,68 @@ __global__ void __launch_bounds__(pq_max_warps<kUnroll>() * 32, 1) linear_persis
     const int step = gridDim.x * a.groups;
 
     ptx::griddep_launch_dependents();
+    const int csize = a.cluster;
+    if (csize > 1) ptx::cluster_arrive_relaxed();  // this CTA has started (its shared memory takes peer stores)
     // Everything that needs the previous grid's output, run by every thread
-    // exactly once: the wait, the quantisation of every 1x128 group of the M
-    // tokens with the activation kernel's group code, and the CTA barrier
-    // after which the codes are read. Group i goes to half-warp slot
+    // exactly once: the wait, the quantisation of the 1x128 groups of the M
+    // tokens with the activation kernel's group code, and the barrier after
+    // which the codes are read. In a cluster of C CTAs, CTA r quantises
+    // groups r, r + C, ... and stores each group's codes and scale into the
+    // shared memory of every CTA of the cluster (itself included), so each
+    // SM does 1/C of the work; the cluster barrier then orders those stores
+    // before any read. Within a CTA, its i-th group goes to half-warp slot
     // i % (2 nwarps), so every warp shares the work, and a slot's groups of
     // one pass (pq_quant_unroll) have their loads issued together.
     auto prologue = [&]() {
         ptx::griddep_wait();
+        const int rank = csize > 1 ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+        if (csize > 1) ptx::cluster_wait();  // every peer has started
         const int half = lane >> 4, hl = lane & 15;
         const int ngroups = a.M * a.KB;
+        const int mine = (ngroups - rank + csize - 1) / csize;  // groups rank, rank + C, ... < ngroups
         const int slots = 2 * nwarps;
         const int slot = 2 * warp + half;
         const uint4 zero = make_uint4(0, 0, 0, 0);
         constexpr int kQU = pq_quant_unroll<kUnroll>();
-        for (int base = 0; base < ngroups; base += kQU * slots) {
+        for (int base = 0; base < mine; base += kQU * slots) {
             uint4 v[kQU];
 #pragma unroll
             for (int u = 0; u < kQU; ++u) {
-                const int gi = base + u * slots + slot;
-                const bool ok = gi < ngroups;
+                const int li = base + u * slots + slot;
+                const bool ok = li < mine;
+                const int gi = rank + li * csize;
                 const int r = ok ? gi / a.KB : 0, kb = ok ? gi % a.KB : 0;
                 v[u] = ok ? ld_dep_stream_v4(a.x + (static_cast<int64_t>(r) * a.K + kb * kGroup + 8 * hl) * 2) : zero;
             }
 #pragma unroll
             for (int u = 0; u < kQU; ++u) {
-                if (base + u * slots + 2 * warp >= ngroups) break;  // warp-uniform: the group code shuffles
-                const int gi = base + u * slots + slot;
-                const bool ok = gi < ngroups;
+                if (base + u * slots + 2 * warp >= mine) break;  // warp-uniform: the group code shuffles
+                const int li = base + u * slots + slot;
+                const bool ok = li < mine;
+                const int gi = rank + li * csize;
                 const int r = ok ? gi / a.KB : 0, kb = ok ? gi % a.KB : 0;
                 uint2 codes;
                 const float sg = quant_group_halfwarp(v[u], codes);
                 if (ok) {
-                    *reinterpret_cast<uint2*>(q_s + r * pq_codes_stride(a.K) + kb * kGroup + 8 * hl) = codes;
-                    if (hl == 0) sa_s[r * a.KB + kb] = sg;
+                    uint8_t* const qd = q_s + r * pq_codes_stride(a.K) + kb * kGroup + 8 * hl;
+                    float* const sd = sa_s + r * a.KB + kb;
+                    if (csize == 1) {
+                        *reinterpret_cast<uint2*>(qd) = codes;
+                        if (hl == 0) *sd = sg;
+                    } else {
+                        const uint32_t qa = ptx::smem_u32(qd), sda = ptx::smem_u32(sd);
+                        for (int c = 0; c < csize; ++c) {
+                            ptx::st_shared_cluster_v2(ptx::mapa_shared(qa, c), codes);
+                            if (hl == 0) ptx::st_shared_cluster_f32(ptx::mapa_shared(sda, c), sg);
+                        }
+                    }
                 }
             }
         }
-        __syncthreads();
+        if (csize > 1)
+            ptx::cluster_sync();
+        else
+            __syncthreads();
     };
     float(*const red)[16][8] = red_all + group * a.wg;
     const int first = blockIdx.x * a.groups + group;
@@ -748,7 +794,7 @@ __global__ void __launch_bounds__(pq_max_warps<kUnroll>() * 32, 1) linear_persis
 }
 
 template <bool kF32Out, int kUnroll, bool kWide>
-cudaError_t launch_persistent(const PqArgs& a, int grid, size_t smem, cudaStream_t stream) {
+cudaError_t configure_persistent() {
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -759,16 +805,65 @@ cudaError_t launch_persistent(const PqArgs& a, int grid, size_t smem, cudaStream
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_release);
     }
+    return cudaSuccess;
+}
+
+// Clusters of `csize` CTAs of the per-SM fused kernel that the device holds
+// at once (one CTA per SM; a cluster's CTAs share a GPC, so for csize > 2
+// some SMs may stay out), from the occupancy API, cached per device.
+template <bool kF32Out, int kUnroll, bool kWide>
+int persistent_clusters(int csize) {
+    static std::atomic<int> cache[64][4];  // csize 1, 2, 4, 8; 1 + clusters, 0 = unknown
+    const int ci = csize >= 8 ? 3 : csize >= 4 ? 2 : csize >= 2 ? 1 : 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int cached = cache[dev & 63][ci].load(std::memory_order_relaxed);
+    if (cached == 0) {
+        int n = 0;
+        if (configure_persistent<kF32Out, kUnroll, kWide>() == cudaSuccess) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(csize);
+            q.blockDim = dim3(pq_max_warps<kUnroll>() * 32);
+            q.dynamicSmemBytes = 227 * 1024;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = csize;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, linear_persistent_kernel<kF32Out, kUnroll, kWide>, &q) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+        } else {
+            cudaGetLastError();
+        }
+        cached = n + 1;
+        cache[dev & 63][ci].store(cached, std::memory_order_relaxed);
+    }
+    return cached - 1;
+}
+
+template <bool kF32Out, int kUnroll, bool kWide>
+cudaError_t launch_persistent(const PqArgs& a, int grid, size_t smem, cudaStream_t stream) {
+    const cudaError_t e = configure_persistent<kF32Out, kUnroll, kWide>();
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(a.groups * a.wg * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = a.cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = a.cluster > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, linear_persistent_kernel<kF32Out, kUnroll, kWide>, a);
 }
 
@@ -920,7 +1015,24 @@ cudaError_t launch_persistent_typed(const void* x, const uint8_t* w, const float
     const size_t smem = pq_smem_bytes(M, K, groups, wv);
     if (smem > 227 * 1024) return cudaErrorNotSupported;
     const int64_t want = (static_cast<int64_t>(a.tiles) + groups - 1) / groups;
-    const int grid = static_cast<int>(want < num_sms ? want : num_sms);
+    int grid = static_cast<int>(want < num_sms ? want : num_sms);
+    // Share the quantisation over a cluster when each SM would otherwise
+    // quantise many groups. The grid becomes whole clusters, all resident at
+    // once (CTAs past the last tile only quantise their share): rounded up,
+    // or down to the resident clusters when that leaves no CTA group more
+    // tiles than before; otherwise a smaller cluster.
+    a.cluster = 1;
+    const int64_t per_cta = static_cast<int64_t>(groups);
+    const int64_t rounds = (a.tiles + grid * per_cta - 1) / (grid * per_cta);
+    for (int c = pq_cluster_size(M, a.KB); c > 1; c /= 2) {
+        const int resident = persistent_clusters<kF32Out, kUnroll, kWide>(c) * c;
+        const int up = (grid + c - 1) / c * c;
+        const int g = up <= resident ? up : resident;
+        if (g < c || (a.tiles + g * per_cta - 1) / (g * per_cta) > rounds) continue;
+        a.cluster = c;
+        grid = g;
+        break;
+    }
     return launch_persistent<kF32Out, kUnroll, kWide>(a, grid, smem, stream);
 }
 

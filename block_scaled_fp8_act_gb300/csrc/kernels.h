@@ -56,8 +56,9 @@ cudaError_t launch_gemm_skinny_grouped(const GemmProblem* probs, int count, bool
 
 // Fused activation quantisation + block GEMM for small M: bf16 x [M, K] in,
 // out [M, N] as fp8_block_gemm(fp8_act_quant(x)) would give. M <= 8: one
-// CTA per SM quantises all the tokens once into shared memory, then warp
-// groups stream the tiles; otherwise (or when the codes do not fit) each
+// CTA per SM quantises all the tokens once into shared memory (from M = 2 a
+// cluster of 2 or 4 CTAs splits that work), then warp groups stream
+// the tiles; otherwise (or when the codes do not fit) each
 // warp quantises the groups of the K blocks it multiplies into its
 // shared-memory slice; fused_fits() tells whether min(8, M) rows of every
 // block fit that kernel's shared-memory ceiling.

@@ -184,6 +184,21 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
+// Stores into a (possibly peer) CTA's shared memory at a mapa_shared address.
+__device__ __forceinline__ void st_shared_cluster_v2(uint32_t addr, uint2 v) {
+    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// The cluster barrier in two halves: arrive (no memory ordering: it only
+// says that this CTA has started) and, later, wait for every CTA's arrival.
+// A CTA may store into a peer's shared memory only once the peer has
+// started, so a kernel arrives early and waits before its first remote store.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
 // Bulk (non-tensor) copies through the TMA engine. Addresses 16-byte aligned,
 // sizes a multiple of 16 bytes.
