@@ -120,6 +120,7 @@ def load_peaks() -> tuple[dict, str]:
 KERNEL_SOURCES = {
     "gemm_skinny_kernel": ("gemm_skinny.cu", "act_group.cuh", "common.cuh", "sm100_ptx.cuh"),
     "gemm_skinny_grouped_kernel": ("gemm_skinny.cu", "act_group.cuh", "common.cuh", "sm100_ptx.cuh"),
+    "linear_persistent_kernel": ("gemm_skinny.cu", "act_group.cuh", "common.cuh", "sm100_ptx.cuh"),
     "gemm_tc_kernel": ("gemm_tc.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
     "gemm_midm_kernel": ("gemm_midm.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
 }
@@ -606,6 +607,8 @@ def main() -> None:
     if (weight_only or fused) and M > 16:
         ap.error("the weight-only and fused workloads are decode paths (M <= 16)")
     kernel = "gemm_skinny_grouped_kernel" if grouped else gemm_kernel_name(M)
+    if fused and M <= 8:
+        kernel = "linear_persistent_kernel"  # the fused call's one-CTA-per-SM kernel
     if args.workload in WORKLOAD_SHAPES:
         shapes, seeds = WORKLOAD_SHAPES[args.workload]
         weights = Weights(device, shapes=shapes, seed_index=seeds)
