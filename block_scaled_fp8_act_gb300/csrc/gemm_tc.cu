@@ -387,7 +387,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
         __syncthreads();
         float* red = reinterpret_cast<float*>(base_ptr);
         const bool ok = *abort == 0;
-        if (epi) {
+        const int vrows = a.M - m0 < BM ? a.M - m0 : BM;  // token rows of the tile that exist
+        if (epi && row < vrows) {
 #pragma unroll
             for (int j = 0; j < C::kCols; j += 4)
                 *reinterpret_cast<float4*>(red + row * C::kRedStride + hf * C::kCols + j) =
@@ -395,32 +396,48 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(const _
         }
         __syncwarp();  // barrier.cluster.*.aligned: the whole warp arrives together
         ptx::cluster_sync();
-        if (epi) {
-            // 4 consecutive columns per element; every peer's load in flight before the sum
+        {
+            // CTA r sums rows [vrows r / S, vrows (r + 1) / S) of every peer's partial (the
+            // tile's real token rows only), 4 consecutive columns per element, in rank order.
+            // Distributed shared memory moves ~15 B per clock per SM whatever the access
+            // style (loads, bulk copies or st.async, measured with every SM busy), so the
+            // bytes that cross it set the time: vrows x BN x 4 per CTA. Every thread of the
+            // CTA takes part, two elements at a time with every peer's load in flight.
             constexpr int kMaxSplits = 8;
-            const int r_begin = split * BM / splits;
-            const int r_end = (split + 1) * BM / splits;
-            const int tid = threadIdx.x - 32 * C::kCtrlWarps;
+            constexpr int kBatch = 2;
+            const int r_begin = split * vrows / splits;
+            const int r_end = (split + 1) * vrows / splits;
             const int elems = (r_end - r_begin) * (BN / 4);
-            for (int e = tid; e < elems; e += kEpiWarps * 32) {
-                const int r = r_begin + e / (BN / 4);
-                const int col = 4 * (e % (BN / 4));
-                const uint32_t local = ptx::smem_u32(red + r * C::kRedStride + col);
-                float4 part[kMaxSplits];
+#pragma unroll 1
+            for (int e0 = threadIdx.x; e0 < elems; e0 += kBatch * C::kThreads) {
+                float4 part[kBatch][kMaxSplits];
 #pragma unroll
-                for (int c = 0; c < kMaxSplits; ++c)
-                    if (c < splits) part[c] = ptx::ld_shared_cluster_v4(ptx::mapa_shared(local, c));
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int u = 0; u < kBatch; ++u) {
+                    const int e = e0 + u * C::kThreads < elems ? e0 + u * C::kThreads : e0;
+                    const int r = r_begin + e / (BN / 4);
+                    const int col = 4 * (e % (BN / 4));
+                    const uint32_t local = ptx::smem_u32(red + r * C::kRedStride + col);
 #pragma unroll
-                for (int c = 0; c < kMaxSplits; ++c)
-                    if (c < splits) {
-                        v.x += part[c].x;
-                        v.y += part[c].y;
-                        v.z += part[c].z;
-                        v.w += part[c].w;
-                    }
-                const int m = m0 + r, n = n0 + col;
-                if (ok && m < a.M) {
+                    for (int c = 0; c < kMaxSplits; ++c)
+                        if (c < splits) part[u][c] = ptx::ld_shared_cluster_v4(ptx::mapa_shared(local, c));
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int e = e0 + u * C::kThreads;
+                    if (e >= elems) continue;
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int c = 0; c < kMaxSplits; ++c)
+                        if (c < splits) {
+                            v.x += part[u][c].x;
+                            v.y += part[u][c].y;
+                            v.z += part[u][c].z;
+                            v.w += part[u][c].w;
+                        }
+                    const int r = r_begin + e / (BN / 4);
+                    const int col = 4 * (e % (BN / 4));
+                    const int m = m0 + r, n = n0 + col;
+                    if (!ok) continue;
                     const int64_t o = static_cast<int64_t>(m) * a.ldo + n;
                     if (n + 3 < a.N && (a.ldo & 3) == 0) {
                         if constexpr (kF32Out) {
