@@ -28,7 +28,8 @@ lmhead` times one vocabulary-sized head (N = 151936, K = 5120) at M = 1.
 `--workload decode-fused` runs one fused fp8_linear launch per shape (the
 activation quantisation inside the GEMM kernel).
 `--workload decode-grouped` runs the five projections as independent problems
-of one grouped act-quant launch and one grouped GEMM launch.
+of one grouped act-quant launch and one grouped GEMM launch; `--workload
+batched-grouped` does the same at M = 102 (the grouped tile kernel).
 `--impl reference` times the CPU oracle instead (the reference arm).
 """
 from __future__ import annotations
@@ -71,8 +72,10 @@ WORKLOADS = {
                         "(one fp8_linear launch per shape: act quant inside the block-FP8 GEMM)", "hbm"),
     "decode-grouped": (1, "grouped decode M={M}: the five dense-27B projection shapes as independent problems, "
                           "one grouped act-quant launch + one grouped block-FP8 GEMM launch", "hbm"),
+    "batched-grouped": (102, "grouped batched decode M={M}: the five dense-27B projection shapes as independent "
+                             "problems, one grouped act-quant launch + one grouped block-FP8 GEMM launch", "hbm"),
 }
-GROUPED = {"decode-grouped"}
+GROUPED = {"decode-grouped", "batched-grouped"}
 # Workloads on other shapes than the five projections: (shapes, weight seed indices).
 WORKLOAD_SHAPES = {"lmhead": ((inputs.VOCAB_SHAPE,), (inputs.VOCAB_SEED_INDEX,))}
 WEIGHT_ONLY = {"decode-w8a16"}
@@ -122,6 +125,7 @@ KERNEL_SOURCES = {
     "gemm_skinny_grouped_kernel": ("gemm_skinny.cu", "act_group.cuh", "common.cuh", "sm100_ptx.cuh"),
     "linear_persistent_kernel": ("gemm_skinny.cu", "act_group.cuh", "common.cuh", "sm100_ptx.cuh"),
     "gemm_tc_kernel": ("gemm_tc.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
+    "gemm_tc_grouped_kernel": ("gemm_tc.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
     "gemm_midm_kernel": ("gemm_midm.cu", "common.cuh", "sm100_ptx.cuh", "tc_ptx.cuh"),
 }
 
@@ -606,7 +610,8 @@ def main() -> None:
     fused = args.workload in FUSED
     if (weight_only or fused) and M > 16:
         ap.error("the weight-only and fused workloads are decode paths (M <= 16)")
-    kernel = "gemm_skinny_grouped_kernel" if grouped else gemm_kernel_name(M)
+    kernel = ("gemm_skinny_grouped_kernel" if M <= 16 else "gemm_tc_grouped_kernel") if grouped \
+        else gemm_kernel_name(M)
     if fused and M <= 8:
         kernel = "linear_persistent_kernel"  # the fused call's one-CTA-per-SM kernel
     if args.workload in WORKLOAD_SHAPES:

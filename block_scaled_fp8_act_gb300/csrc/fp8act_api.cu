@@ -87,6 +87,7 @@ int gemm_common(const void* q, const float* sa, const void* w, const float* sw, 
 }
 
 constexpr int kMaxGrouped = 16;
+constexpr int kTileGroupMaxM = 128;  // one token tile: the grouped tile launch takes these
 
 // The single-call checks of one GEMM problem (no launch); OK for an empty one.
 int check_gemm(const fp8act_gemm_problem& p) {
@@ -123,13 +124,38 @@ int gemm_grouped_common(const fp8act_gemm_problem* problems, int count, bool out
                               p.sw, p.out, p.M, p.N, p.K};
     }
     if (int e = launch_status(fp8act::launch_gemm_skinny_grouped(skinny, n_skinny, out_f32, s))) return e;
+    auto one = [&](const fp8act::GemmProblem& p) {
+        return launch_status(launch_gemm_any(p.q, p.sa, p.w, p.sw, p.M, p.N, p.K, p.out, out_f32, sms, s));
+    };
+    // Batched widths (one token tile each): one grouped tile launch per chunk
+    // whose weight tiles fill the SMs (no split K, no launch per problem); a
+    // chunk with fewer tiles, and M > 128, one launch per problem.
+    fp8act::GemmProblem tiled[kMaxGrouped];
+    int n_tiled = 0;
     for (int i = 0; i < count; ++i) {
         const fp8act_gemm_problem& p = problems[i];
         if (p.M <= kSkinnyMaxM || p.N == 0) continue;
-        if (int e = launch_status(launch_gemm_any(static_cast<const uint8_t*>(p.q_e4m3), p.sa,
-                                                  static_cast<const uint8_t*>(p.w_e4m3), p.sw, p.M, p.N, p.K, p.out,
-                                                  out_f32, sms, s)))
+        const fp8act::GemmProblem g = {static_cast<const uint8_t*>(p.q_e4m3), p.sa,
+                                       static_cast<const uint8_t*>(p.w_e4m3), p.sw, p.out, p.M, p.N, p.K};
+        if (p.M > kTileGroupMaxM) {
+            if (int e = one(g)) return e;
+        } else {
+            tiled[n_tiled++] = g;
+        }
+    }
+    const int cap = fp8act::gemm_tc_grouped_capacity();
+    for (int c0 = 0; c0 < n_tiled; c0 += cap) {
+        const int n = n_tiled - c0 < cap ? n_tiled - c0 : cap;
+        int64_t tiles = 0;
+        for (int j = 0; j < n; ++j) tiles += (tiled[c0 + j].N + 127) / 128;
+        const cudaError_t g =
+            tiles >= sms ? fp8act::launch_gemm_tc_grouped(tiled + c0, n, out_f32, sms, s) : cudaErrorNotSupported;
+        if (g == cudaErrorNotSupported) {  // too few tiles to fill the SMs (or too many to list)
+            for (int j = 0; j < n; ++j)
+                if (int e = one(tiled[c0 + j])) return e;
+        } else if (int e = launch_status(g)) {
             return e;
+        }
     }
     return FP8ACT_OK;
 }

@@ -45,6 +45,7 @@
 // issuing work, the producer waits (bounded) for the copies it already
 // issued, the MMA thread for the MMAs it already issued, and only then is
 // TMEM freed and the CTA leaves (never a hang, no copy or MMA in flight at exit).
+#include <algorithm>
 #include <atomic>
 
 #include "common.cuh"
@@ -544,6 +545,318 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const TcA
     return cudaLaunchKernelEx(&cfg, kernel, ta, tb, args);
 }
 
+// ------------------------------------------------------------------------
+// Grouped batched decode: several problems of one token tile each
+// (16 < M <= 128) in one persistent launch of the 128 x 128 tile kernel.
+// The problems' weight tiles form one list, problems in order of falling K
+// (a tile costs its K groups). With G CTAs the list runs in whole rounds of
+// G tiles, CTA b taking position r G + b in even rounds r and r G + G - 1 - b
+// in odd ones (a snake, so the costly first tiles spread over all CTAs); the
+// tiles of the last, partial round go, largest first, to the CTAs with the
+// fewest K groups so far (the host works that out; the kernel gets each
+// CTA's leftover tile). The tiles of several projections fill the grid without splitting
+// K, so there is no cross-CTA reduction (on one N = 5120 projection alone
+// that reduction is a third of the launch), and the stage ring and the two
+// accumulators run on across the tiles of different problems. Each problem
+// has its own tensor maps in the kernel parameters. Roles, barriers, bounded
+// waits and the drain are those of gemm_tc_kernel.
+constexpr int kMaxTcGroup = 8;        // problems per launch (their tensor maps travel in the parameters)
+constexpr int kMaxTcGroupCtas = 256;  // grid limit of the grouped launch
+
+struct TcGroupProblem {
+    const float* sa;
+    const float* sw;
+    void* out;
+    int M, N, KB;
+    int tile_begin;  // list position of this problem's first tile
+};
+
+struct TcGroupedArgs {
+    CUtensorMap ta[kMaxTcGroup];  // activation codes [M, K], 128 x 128 boxes
+    CUtensorMap tb[kMaxTcGroup];  // weight codes [N, K], 128 x 128 boxes
+    TcGroupProblem p[kMaxTcGroup];
+    int count;
+    int tiles;                   // list length
+    int full_rounds;             // tiles / G
+    unsigned long long wait_ns;  // bound of every wait that can give up (test hook shortens it)
+    int withhold;                // test hook: the producer never issues the CTA's first K group
+    short leftover[kMaxTcGroupCtas];  // CTA b's tile of the partial last round, or -1
+};
+
+__host__ __device__ __forceinline__ int grouped_position(int round, int b, int G) {
+    return round * G + ((round & 1) ? G - 1 - b : b);
+}
+
+// The j-th tile of CTA b, or -1 past its last.
+__device__ __forceinline__ int grouped_tile(const TcGroupedArgs& a, int j, int b, int G) {
+    if (j < a.full_rounds) return grouped_position(j, b, G);
+    return j == a.full_rounds ? a.leftover[b] : -1;
+}
+
+__device__ __forceinline__ int grouped_problem(const TcGroupedArgs& a, int t) {
+    int p = 0;
+    while (p + 1 < a.count && t >= a.p[p + 1].tile_begin) ++p;
+    return p;
+}
+
+// The producer's walk over this CTA's (tile, K group) units.
+struct GroupedCursor {
+    int j, t, p, kb;
+    __device__ __forceinline__ void start(const TcGroupedArgs& a, int b, int G) {
+        j = 0;
+        t = grouped_tile(a, 0, b, G);
+        p = t >= 0 ? grouped_problem(a, t) : 0;
+        kb = 0;
+    }
+    __device__ __forceinline__ void next(const TcGroupedArgs& a, int b, int G) {
+        if (++kb == a.p[p].KB) {
+            kb = 0;
+            t = grouped_tile(a, ++j, b, G);
+            if (t >= 0) p = grouped_problem(a, t);
+        }
+    }
+    __device__ __forceinline__ int n0(const TcGroupedArgs& a) const { return (t - a.p[p].tile_begin) * 128; }
+};
+
+template <bool kF32Out>
+__global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
+    gemm_tc_grouped_kernel(const __grid_constant__ TcGroupedArgs a) {
+    constexpr int BN = 128;
+    using C = TcCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* const base_ptr = smem_raw + (base - ptx::smem_u32(smem_raw));
+    const uint32_t bar0 = base + C::kStages * C::kStageBytes;
+    const uint32_t full0 = bar0;                       // [kStages] TMA landed
+    const uint32_t empty0 = full0 + 8 * C::kStages;    // [kStages] MMAs done reading
+    const uint32_t tfull0 = empty0 + 8 * C::kStages;   // [2] accumulator ready
+    const uint32_t tempty0 = tfull0 + 16;              // [2] accumulator drained
+    const uint32_t drain = tempty0 + 16;               // MMA thread: every issued MMA has completed
+    const uint32_t tmem_slot = drain + 8;
+    volatile uint32_t* const tmem_slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+    volatile int* const abort = reinterpret_cast<volatile int*>(base_ptr + (tmem_slot - base) + 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = static_cast<int>(gridDim.x);
+    const int b = static_cast<int>(blockIdx.x);
+    int total = 0;  // K groups this CTA streams
+    for (int j = 0;; ++j) {
+        const int t = grouped_tile(a, j, b, G);
+        if (t < 0) break;
+        total += a.p[grouped_problem(a, t)].KB;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(full0 + 8 * s, 1);
+            ptx::mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(tfull0 + 8 * i, 1);
+            ptx::mbar_init(tempty0 + 8 * i, kEpiWarps);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, C::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            ptx::griddep_launch_dependents();
+            for (int p = 0; p < a.count; ++p) {
+                ptx::prefetch_tensormap(&a.ta[p]);
+                ptx::prefetch_tensormap(&a.tb[p]);
+            }
+            const uint64_t pol_w = ptx::policy_evict_first();  // every weight tile is read once
+            const uint64_t pol_q = ptx::policy_evict_last();   // a problem's codes are re-read by its tiles
+            const bool skip0 = a.withhold != 0;
+            const int pre = total < C::kStages ? total : C::kStages;
+            GroupedCursor cw;  // weights: independent of the previous grid
+            cw.start(a, b, G);
+            for (int i = 0; i < pre; ++i, cw.next(a, b, G)) {
+                if (skip0 && i == 0) continue;
+                ptx::mbar_arrive_expect_tx(full0 + 8 * i, C::kStageBytes);
+                ptx::tma_load_2d(base + i * C::kStageBytes + kABytes, &a.tb[cw.p], full0 + 8 * i, cw.kb * kGroup,
+                                 cw.n0(a), pol_w);
+            }
+            ptx::griddep_wait();  // the activation codes are the previous grid's output
+            GroupedCursor ca;
+            ca.start(a, b, G);
+            for (int i = 0; i < pre; ++i, ca.next(a, b, G)) {
+                if (skip0 && i == 0) continue;
+                ptx::tma_load_2d(base + i * C::kStageBytes, &a.ta[ca.p], full0 + 8 * i, ca.kb * kGroup, 0, pol_q);
+            }
+            int issued = pre;
+            for (int i = pre; i < total; ++i, cw.next(a, b, G)) {
+                const int s = i % C::kStages;
+                if (!ptx::mbar_wait_or_abort(empty0 + 8 * s, ((i / C::kStages) - 1) & 1, a.wait_ns, abort)) {
+                    fail(abort, 1u);
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
+                ptx::tma_load_2d(base + s * C::kStageBytes + kABytes, &a.tb[cw.p], full0 + 8 * s, cw.kb * kGroup,
+                                 cw.n0(a), pol_w);
+                ptx::tma_load_2d(base + s * C::kStageBytes, &a.ta[cw.p], full0 + 8 * s, cw.kb * kGroup, 0, pol_q);
+                issued = i + 1;
+            }
+            // Every copy issued must land before the CTA may leave.
+            for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+                if (!(skip0 && i == 0) && !ptx::mbar_wait(full0 + 8 * (i % C::kStages), (i / C::kStages) & 1))
+                    fail(abort, 16u);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_e4m3_f32(BM, BN);
+            for (int i = 0; i < total; ++i) {
+                const int s = i % C::kStages;
+                const int acc_b = i & 1;
+                if (!ptx::mbar_wait_or_abort(full0 + 8 * s, (i / C::kStages) & 1, a.wait_ns, abort)) {
+                    fail(abort, 2u);
+                    break;
+                }
+                if (i >= 2 && !ptx::mbar_wait_or_abort(tempty0 + 8 * acc_b, ((i >> 1) - 1) & 1, a.wait_ns, abort)) {
+                    fail(abort, 4u);
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t a_tile = base + s * C::kStageBytes;
+                const uint32_t b_tile = a_tile + kABytes;
+#pragma unroll
+                for (int k = 0; k < kGroup / 32; ++k)
+                    tc::mma_f8f6f4(tmem_base + acc_b * BN, tc::desc_kmajor_sw128(a_tile + 32 * k),
+                                   tc::desc_kmajor_sw128(b_tile + 32 * k), idesc, k > 0 ? 1u : 0u);
+                tc::commit(empty0 + 8 * s);       // the stage's smem may be refilled once these MMAs finish
+                tc::commit(tfull0 + 8 * acc_b);   // the accumulator holds this K group's product
+            }
+            // No MMA may still run when TMEM is freed or the CTA leaves.
+            tc::commit(drain);
+            if (!ptx::mbar_wait(drain, 0)) fail(abort, 32u);
+        }
+    } else {
+        // ------------------------------------------------------- epilogue
+        ptx::griddep_wait();  // scales come from the previous grid; it may still read `out`
+        const int qd = warp & 3;                     // TMEM lane quadrant this warp may access
+        const int hf = (warp - C::kCtrlWarps) >> 2;  // column half
+        const int row = qd * 32 + lane;              // token
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + hf * C::kCols;
+        float acc[C::kCols];
+        bool failed = false;
+        int i = 0;  // accumulator uses so far
+        for (int j = 0; !failed; ++j) {
+            const int t = grouped_tile(a, j, b, G);
+            if (t < 0) break;
+            const TcGroupProblem& pr = a.p[grouped_problem(a, t)];
+            const int n0 = (t - pr.tile_begin) * BN;
+            const int nb = (n0 + hf * C::kCols) / kGroup;
+            const bool row_ok = row < pr.M && n0 + hf * C::kCols < pr.N;
+            const float* sa_row = pr.sa + static_cast<int64_t>(row_ok ? row : 0) * pr.KB;
+            const float* sw_row = pr.sw + static_cast<int64_t>(row_ok ? nb : 0) * pr.KB;
+#pragma unroll
+            for (int j = 0; j < C::kCols; ++j) acc[j] = 0.f;
+            for (int k = 0; k < pr.KB; ++k, ++i) {
+                const int acc_b = i & 1;
+                const float scale = row_ok ? ld_dep_f32(sa_row + k) * __ldg(sw_row + k) : 0.f;
+                // the whole warp decides together (tcgen05.ld is warp-collective)
+                if (!__all_sync(0xffffffffu,
+                                ptx::mbar_wait_or_abort(tfull0 + 8 * acc_b, (i >> 1) & 1, a.wait_ns, abort))) {
+                    if (lane == 0) fail(abort, 8u);
+                    failed = true;
+                    break;
+                }
+                tc::fence_after_sync();
+                uint32_t r0[32], r1[32];
+                tc::ld_32x32b_x32(t_row + acc_b * BN, r0);
+                tc::ld_32x32b_x32(t_row + acc_b * BN + 32, r1);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    fma2(acc[j], acc[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), scale);
+                    fma2(acc[32 + j], acc[33 + j], __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]), scale);
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(tempty0 + 8 * acc_b);
+            }
+            if (row < pr.M && !failed) {
+                const int nstart = n0 + hf * C::kCols;
+                if constexpr (kF32Out) {
+                    float* dst = static_cast<float*>(pr.out) + static_cast<int64_t>(row) * pr.N + nstart;
+                    if ((pr.N & 3) == 0 && nstart + C::kCols <= pr.N) {
+#pragma unroll
+                        for (int j = 0; j < C::kCols; j += 4)
+                            *reinterpret_cast<float4*>(dst + j) =
+                                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < C::kCols; ++j)
+                            if (nstart + j < pr.N) dst[j] = acc[j];
+                    }
+                } else {
+                    __nv_bfloat16* dst =
+                        static_cast<__nv_bfloat16*>(pr.out) + static_cast<int64_t>(row) * pr.N + nstart;
+                    if ((pr.N & 7) == 0 && nstart + C::kCols <= pr.N) {
+#pragma unroll
+                        for (int j = 0; j < C::kCols; j += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(acc[j], acc[j + 1]);
+                            v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+                            v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+                            v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+                            *reinterpret_cast<uint4*>(dst + j) = v;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < C::kCols; ++j)
+                            if (nstart + j < pr.N) dst[j] = __float2bfloat16_rn(acc[j]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 1) tc::tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+template <bool kF32Out>
+cudaError_t launch_grouped_typed(const TcGroupedArgs& args, int grid, cudaStream_t stream) {
+    using C = TcCfg<128>;
+    auto kernel = gemm_tc_grouped_kernel<kF32Out>;
+    static std::atomic<uint64_t> configured{0};  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_release);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
 }  // namespace
 
 unsigned int read_and_clear_tc_error() {
@@ -619,6 +932,71 @@ cudaError_t launch_gemm_tc(const uint8_t* q, const float* sa, const uint8_t* w, 
         return launch_cols(128, n_split, N - n_split);
     }
     return launch_cols(256, 0, N);
+}
+
+int gemm_tc_grouped_capacity() { return kMaxTcGroup; }
+
+cudaError_t launch_gemm_tc_grouped(const GemmProblem* probs, int count, bool out_f32, int num_sms,
+                                   cudaStream_t stream) {
+    if (count <= 0) return cudaSuccess;
+    if (count > kMaxTcGroup) return cudaErrorInvalidValue;
+    // problems in order of falling K: a tile's cost is its K groups
+    int order[kMaxTcGroup];
+    for (int i = 0; i < count; ++i) order[i] = i;
+    for (int i = 1; i < count; ++i)
+        for (int j = i; j > 0 && probs[order[j - 1]].K < probs[order[j]].K; --j) {
+            const int tmp = order[j];
+            order[j] = order[j - 1];
+            order[j - 1] = tmp;
+        }
+    TcGroupedArgs a = {};
+    int tiles = 0;
+    for (int i = 0; i < count; ++i) {
+        const GemmProblem& src = probs[order[i]];
+        if (src.M < 1 || src.M > BM || src.N < 1) return cudaErrorInvalidValue;
+        if (!encode_tmap_2d_u8(&a.ta[i], src.q, static_cast<uint64_t>(src.K), static_cast<uint64_t>(src.M),
+                               static_cast<uint64_t>(src.K), kGroup, BM, true) ||
+            !encode_tmap_2d_u8(&a.tb[i], src.w, static_cast<uint64_t>(src.K), static_cast<uint64_t>(src.N),
+                               static_cast<uint64_t>(src.K), kGroup, 128, true))
+            return cudaErrorInvalidValue;
+        TcGroupProblem& d = a.p[i];
+        d.sa = src.sa;
+        d.sw = src.sw;
+        d.out = src.out;
+        d.M = src.M;
+        d.N = src.N;
+        d.KB = src.K / kGroup;
+        d.tile_begin = tiles;
+        tiles += (src.N + 127) / 128;
+    }
+    if (tiles > 32767) return cudaErrorNotSupported;  // leftover tiles are recorded as 16-bit positions
+    a.count = count;
+    a.tiles = tiles;
+    a.wait_ns = tile_wait_limit_ns();
+    a.withhold = tile_withhold_first_load() ? 1 : 0;
+    int grid = tiles < num_sms ? tiles : num_sms;
+    if (grid > kMaxTcGroupCtas) grid = kMaxTcGroupCtas;
+    // Whole snake rounds, then the partial round's tiles (largest first) to
+    // the CTAs with the fewest K groups after the whole rounds.
+    a.full_rounds = tiles / grid;
+    const int partial = tiles - a.full_rounds * grid;
+    int kb_of[kMaxTcGroup + 1];
+    for (int i = 0; i < count; ++i) kb_of[i] = a.p[i].KB;
+    auto cost = [&](int t) {
+        int i = 0;
+        while (i + 1 < count && t >= a.p[i + 1].tile_begin) ++i;
+        return kb_of[i];
+    };
+    int load[kMaxTcGroupCtas], by_load[kMaxTcGroupCtas];
+    for (int c = 0; c < grid; ++c) {
+        load[c] = 0;
+        for (int r = 0; r < a.full_rounds; ++r) load[c] += cost(grouped_position(r, c, grid));
+        by_load[c] = c;
+        a.leftover[c] = -1;
+    }
+    std::stable_sort(by_load, by_load + grid, [&](int x, int y) { return load[x] < load[y]; });
+    for (int i = 0; i < partial; ++i) a.leftover[by_load[i]] = static_cast<short>(a.full_rounds * grid + i);
+    return out_f32 ? launch_grouped_typed<true>(a, grid, stream) : launch_grouped_typed<false>(a, grid, stream);
 }
 
 }  // namespace fp8act

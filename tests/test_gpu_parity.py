@@ -346,6 +346,40 @@ def test_gemm_grouped_ragged_mix(fp8act):
     _grouped_compare(fp8act, probs, [m for _, _, m in dims], seed=910)
 
 
+@pytest.mark.parametrize("M", [32, 64, 102, 128])
+def test_gemm_grouped_batched_five_shapes(fp8act, M):
+    """Batched-decode widths over the five projections in one grouped call:
+    their 336 weight tiles fill the SMs, so one persistent launch of the
+    128 x 128 tile kernel takes them all (the tiles dealt over the CTAs in
+    order of falling K, no split K); every output against the oracle."""
+    _grouped_compare(fp8act, [problem(si) for si in range(len(SHAPES))], [M] * len(SHAPES), seed=820 + M)
+
+
+def test_gemm_grouped_batched_ragged(fp8act):
+    """The grouped tile launch with ragged problems: N ending inside a weight
+    tile and inside a scale block, M from 17 to 128, K from 3 to 16 groups,
+    201 tiles in all (past the SM count, so the grouped launch is taken),
+    problems given out of K order."""
+    from parity_util import Problem
+    dims = [(300, 384, 50), (9000, 1024, 100), (1000, 2048, 128), (10000, 640, 17), (5000, 512, 77)]
+    assert sum((N + 127) // 128 for N, _, _ in dims) >= 152
+    probs = [Problem(N, K, seed=940 + i) for i, (N, K, _) in enumerate(dims)]
+    _grouped_compare(fp8act, probs, [m for _, _, m in dims], seed=950)
+
+
+def test_gemm_grouped_batched_equals_single_call_without_split(fp8act):
+    """(17408, 5120) alone runs 136 unsplit tiles, one K order per tile; in a
+    grouped launch with the other projections each of its tiles runs the
+    same K order on some CTA, so the fp32 results are equal bit for bit."""
+    ps = [problem(si) for si in range(len(SHAPES))]
+    acts = [p.activations(102, 970 + i) for i, p in enumerate(ps)]
+    outs32 = fp8act.fp8_block_gemm_grouped_f32([(q, sa, p.w, p.sw) for (q, sa, _, _), p in zip(acts, ps)])
+    q, sa, _, _ = acts[0]
+    single = fp8act.fp8_block_gemm_f32(q, sa, ps[0].w, ps[0].sw)
+    torch.cuda.synchronize()
+    assert ps[0].N == 17408 and torch.equal(outs32[0], single)
+
+
 # ------------------------------------------- fused act-quant + GEMM (fp8_linear)
 def _linear_compare(fp8act, p, M, seed, edge=False):
     from parity_util import compare_gemm
