@@ -83,3 +83,41 @@ def test_zero_wait_limit_stops_anywhere_and_recovers(fp8act, M, N, K):
     assert status in (0, TIMEOUT)
     again = _clean_call_matches_oracle(fp8act, p, q, sa, q_ref, sa_ref)
     assert torch.equal(again, ref32)
+
+
+# Grouped batched decode: three problems whose 190 weight tiles fill the SMs,
+# so one launch of the grouped tile kernel takes them all.
+GROUPED = [(9000, 1024, 100), (10000, 640, 17), (5000, 512, 77)]
+
+
+def _grouped_args(fp8act):
+    from parity_util import Problem
+    probs = [Problem(N, K, seed=N + K + 5) for N, K, _ in GROUPED]
+    acts = [p.activations(M, seed=M + 3) for p, (_, _, M) in zip(probs, GROUPED)]
+    return [(q, sa, p.w, p.sw) for (q, sa, _, _), p in zip(acts, probs)]
+
+
+@pytest.mark.parametrize("withhold,limit", [(True, 1_000_000), (False, 0)])
+def test_grouped_tile_launch_times_out_and_recovers(fp8act, withhold, limit):
+    """The grouped tile kernel's waits are bounded like the single-problem
+    kernel's: with each CTA's first copy withheld (or a zero bound) the launch
+    leaves, the status reports the timeout (withheld) or OK / TIMEOUT (zero
+    bound), and the next grouped call gives the same bits as before with a
+    clean status."""
+    assert sum((N + 127) // 128 for N, _, _ in GROUPED) >= 152
+    args = _grouped_args(fp8act)
+    ref = fp8act.fp8_block_gemm_grouped_f32(args)
+    assert fp8act.check_status() == 0
+    fp8act.set_wait_limit(limit, withhold)
+    try:
+        for _ in range(1 if withhold else 4):
+            fp8act.fp8_block_gemm_grouped_f32(args)
+        status = fp8act.check_status()
+    finally:
+        fp8act.set_wait_limit(-1, False)
+    assert status == TIMEOUT if withhold else status in (0, TIMEOUT)
+    assert fp8act.check_status() == 0
+    again = fp8act.fp8_block_gemm_grouped_f32(args)
+    assert fp8act.check_status() == 0
+    for a, b in zip(ref, again):
+        assert torch.equal(a, b)

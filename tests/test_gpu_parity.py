@@ -367,6 +367,20 @@ def test_gemm_grouped_batched_ragged(fp8act):
     _grouped_compare(fp8act, probs, [m for _, _, m in dims], seed=950)
 
 
+def test_gemm_grouped_every_route_in_one_call(fp8act):
+    """Twelve problems in one grouped call: one at M = 8 (the grouped
+    weight-streaming launch), ten at 17 <= M <= 128 (the first eight, 192
+    tiles, in one grouped tile launch; the last two, too few tiles to fill
+    the SMs, one tile-kernel launch each) and one at M = 200 (its own
+    launch); every output against the oracle."""
+    from parity_util import Problem
+    dims = [(500, 384, 8)] + [(3000, 256, m) for m in (17, 30, 45, 64, 80, 96, 113, 128, 20, 100)] + \
+        [(700, 512, 200)]
+    assert sum((N + 127) // 128 for N, _, m in dims[1:9]) >= 152
+    probs = [Problem(N, K, seed=990 + i) for i, (N, K, _) in enumerate(dims)]
+    _grouped_compare(fp8act, probs, [m for _, _, m in dims], seed=995)
+
+
 def test_gemm_grouped_batched_equals_single_call_without_split(fp8act):
     """(17408, 5120) alone runs 136 unsplit tiles, one K order per tile; in a
     grouped launch with the other projections each of its tiles runs the
