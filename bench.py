@@ -709,58 +709,76 @@ def main() -> None:
             wall = (time.perf_counter() - t0) / max(e2e_steps, 1)
         return max(s0.elapsed_time(s1) / 1e3 / max(e2e_steps, 1), wall)
 
-    def timed_e2e_pipelined() -> float:
-        """Seconds per step with every step's host copies inside the timed region,
-        overlapped with the neighbouring steps' compute (independent batches, as a
-        server streams them): step i uploads its activations into buffer set i % 2
-        on an upload stream, runs its calls on `stream` (the step's CUDA graph) once
-        they have landed and set i % 2's previous outputs have been read back, and
-        downloads its outputs on a download stream. The larger of the event time
-        (first upload to last download) and the host wall time."""
-        sets = [wl, Workload(M, weights, device, weight_only=weight_only, grouped=grouped, fused=fused)]
-        step_graphs = {(b, c): capture(lambda b=b, c=c: sets[b].enqueue_step(c, stream), stream)
-                       for b in range(2) for c in range(wl.copies)}
+    def timed_e2e_pipelined() -> tuple[float, int, int]:
+        """Seconds per step, steps timed and steps per graph, with every step's host
+        copies inside the timed region, overlapped with the neighbouring steps'
+        compute (independent batches, as a server streams them). P steps form one
+        CUDA graph replay (as in the device-timed leg where a step's host copies
+        are at most 2 MB, one step per replay above). Replay r runs
+        on buffer-set group r % 2: its P uploads go out on an upload stream once
+        replay r - 2 has read that group's activations, the replay waits for them
+        and for the group's previous outputs to be back on the host, and its P
+        downloads follow on a download stream. The larger of the event time (first
+        upload to last download) and the host wall time."""
+        per_set = (wl.x_all.numel() + wl.out_all.numel()) * 2
+        # Where a step's copies are large the host link sets the pace and finer
+        # replays overlap it better (measured at M = 102: 2865 GB/s with one step
+        # per replay, 2580 with ten); small copies hide entirely either way and
+        # the longer replays save the per-replay boundary (decode: 4093 against 3911).
+        P = S if per_set <= (2 << 20) else 1
+        groups = [[wl if (g, k) == (0, 0) else
+                   Workload(M, weights, device, weight_only=weight_only, grouped=grouped, fused=fused)
+                   for k in range(P)] for g in range(2)]
+        # replay r: weight copy of its step k is (r P + k) mod copies; the graph depends on
+        # r mod 2 (buffer group) and r P mod copies
+        n_graphs = 2 * wl.copies
+        step_graphs = [capture(lambda j=j: [groups[j % 2][k].enqueue_step((j * P + k) % wl.copies, stream)
+                                            for k in range(P)], stream) for j in range(n_graphs)]
         up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
-        def run(n: int) -> tuple[float, float]:
-            ev_in = [torch.cuda.Event() for _ in range(n)]
-            ev_comp = [torch.cuda.Event() for _ in range(n)]
-            ev_out = [torch.cuda.Event() for _ in range(n)]
+        def run(reps: int) -> tuple[float, float]:
+            ev_in = [torch.cuda.Event() for _ in range(reps)]
+            ev_comp = [torch.cuda.Event() for _ in range(reps)]
+            ev_out = [torch.cuda.Event() for _ in range(reps)]
             s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             s0.record(up)
-            for i in range(n):
-                b, st = i % 2, sets[i % 2]
+            for r in range(reps):
+                sets = groups[r % 2]
                 with torch.cuda.stream(up):
-                    if i >= 2:
-                        up.wait_event(ev_comp[i - 2])  # step i - 2 has read this set's activations
-                    st.x_all.copy_(st.x_host_all, non_blocking=True)
-                    ev_in[i].record(up)
+                    if r >= 2:
+                        up.wait_event(ev_comp[r - 2])  # replay r - 2 has read this group's activations
+                    for st in sets:
+                        st.x_all.copy_(st.x_host_all, non_blocking=True)
+                    ev_in[r].record(up)
                 with torch.cuda.stream(stream):
-                    stream.wait_event(ev_in[i])
-                    if i >= 2:
-                        stream.wait_event(ev_out[i - 2])  # this set's outputs are back on the host
-                    step_graphs[(b, i % wl.copies)].replay()
-                    ev_comp[i].record(stream)
+                    stream.wait_event(ev_in[r])
+                    if r >= 2:
+                        stream.wait_event(ev_out[r - 2])  # this group's outputs are back on the host
+                    step_graphs[r % n_graphs].replay()
+                    ev_comp[r].record(stream)
                 with torch.cuda.stream(down):
-                    down.wait_event(ev_comp[i])
-                    st.out_host_all.copy_(st.out_all, non_blocking=True)
-                    ev_out[i].record(down)
+                    down.wait_event(ev_comp[r])
+                    for st in sets:
+                        st.out_host_all.copy_(st.out_all, non_blocking=True)
+                    ev_out[r].record(down)
             s1.record(down)
             s1.synchronize()
             wall = time.perf_counter() - t0
             return s0.elapsed_time(s1) / 1e3, wall
 
-        run(max(args.warmup, 2))
-        ev_t, wall = run(max(e2e_steps, 1))
-        del step_graphs, sets
-        return max(ev_t, wall) / max(e2e_steps, 1)
+        run(max(-(-args.warmup // P), 2))
+        reps = max(2, -(-e2e_steps // P))
+        ev_t, wall = run(reps)
+        del step_graphs, groups
+        return max(ev_t, wall) / (reps * P), reps * P, P
 
     # Eager: every API call issued from Python each step (binding overhead included).
     t_e2e_eager = max_over_ranks(world, timed_e2e(lambda i: e2e_step(i % wl.copies)))
     # Pipelined: copies on their own streams, overlapping the neighbouring steps' compute.
-    t_e2e_pipe = max_over_ranks(world, timed_e2e_pipelined()) if e2e_steps else float("inf")
+    t_e2e_pipe, e2e_pipe_steps, e2e_pipe_per_graph = timed_e2e_pipelined() if e2e_steps else (float("inf"), 0, 0)
+    t_e2e_pipe = max_over_ranks(world, t_e2e_pipe)
     # Graph: the same calls (copies included) captured once and replayed per step.
     e2e_graphs = [capture(lambda c=c: e2e_step(c), stream) for c in range(wl.copies)]
     t_e2e = max_over_ranks(world, timed_e2e(lambda i: e2e_graphs[i % wl.copies].replay()))
@@ -840,11 +858,12 @@ def main() -> None:
         "e2e": {"value": round(world * step_units / t_e2e_pipe, 2),
                 "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e_pipe * 1e3, 5),
+                "steps": e2e_pipe_steps, "steps_per_graph": e2e_pipe_per_graph,
                 "how": "each step: one H2D copy of all its activations from pinned host memory, the step's "
-                       "API calls (captured once through the public API, one CUDA graph per step), one D2H "
-                       "copy of all its outputs, every copy inside the timed region; uploads and downloads "
-                       "run on their own streams with two buffer sets, so they overlap the neighbouring "
-                       "steps' compute (independent batches)",
+                       "API calls (captured once through the public API), one D2H copy of all its outputs, "
+                       "every copy inside the timed region; steps_per_graph consecutive steps per CUDA graph "
+                       "replay on their own buffer sets, their uploads and downloads on separate streams "
+                       "overlapping the neighbouring replays' compute (independent batches)",
                 "serial": {"value": round(world * step_units / t_e2e, 2), "ms_per_step": round(t_e2e * 1e3, 5),
                            "how": "the same per-step copies and graph on one stream, nothing overlapped"},
                 "eager": {"value": round(world * step_units / t_e2e_eager, 2),
