@@ -29,7 +29,8 @@ lmhead` times one vocabulary-sized head (N = 151936, K = 5120) at M = 1.
 activation quantisation inside the GEMM kernel).
 `--workload decode-grouped` runs the five projections as independent problems
 of one grouped act-quant launch and one grouped GEMM launch; `--workload
-batched-grouped` does the same at M = 102 (the grouped tile kernel).
+batched-grouped` and `--workload prefill-grouped` do the same at M = 102 and
+4096 (the grouped tile kernel).
 `--impl reference` times the CPU oracle instead (the reference arm).
 """
 from __future__ import annotations
@@ -74,8 +75,10 @@ WORKLOADS = {
                           "one grouped act-quant launch + one grouped block-FP8 GEMM launch", "hbm"),
     "batched-grouped": (102, "grouped batched decode M={M}: the five dense-27B projection shapes as independent "
                              "problems, one grouped act-quant launch + one grouped block-FP8 GEMM launch", "hbm"),
+    "prefill-grouped": (4096, "grouped prefill chunk M={M}: the five dense-27B projection shapes as independent "
+                              "problems, one grouped act-quant launch + one grouped block-FP8 GEMM launch", "tensor"),
 }
-GROUPED = {"decode-grouped", "batched-grouped"}
+GROUPED = {"decode-grouped", "batched-grouped", "prefill-grouped"}
 # Workloads on other shapes than the five projections: (shapes, weight seed indices).
 WORKLOAD_SHAPES = {"lmhead": ((inputs.VOCAB_SHAPE,), (inputs.VOCAB_SEED_INDEX,))}
 WEIGHT_ONLY = {"decode-w8a16"}

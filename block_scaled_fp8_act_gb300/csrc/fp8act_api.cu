@@ -127,36 +127,45 @@ int gemm_grouped_common(const fp8act_gemm_problem* problems, int count, bool out
     auto one = [&](const fp8act::GemmProblem& p) {
         return launch_status(launch_gemm_any(p.q, p.sa, p.w, p.sw, p.M, p.N, p.K, p.out, out_f32, sms, s));
     };
-    // Batched widths (one token tile each): one grouped tile launch per chunk
-    // whose weight tiles fill the SMs (no split K, no launch per problem); a
-    // chunk with fewer tiles, and M > 128, one launch per problem.
-    fp8act::GemmProblem tiled[kMaxGrouped];
-    int n_tiled = 0;
+    // Problems of the tile kernel, grouped by width: one token tile each (16 < M
+    // <= 128: 128-wide weight tiles, a chunk is worth one launch once its tiles
+    // fill the SMs) and several (M > 128: 256-wide tiles, once they fill two
+    // waves, the single-problem kernel's own rule for wide tiles). One grouped
+    // persistent launch per chunk of up to gemm_tc_grouped_capacity()
+    // problems; a chunk with fewer tiles, one launch per problem.
+    fp8act::GemmProblem narrow[kMaxGrouped], wide[kMaxGrouped];
+    int n_narrow = 0, n_wide = 0;
     for (int i = 0; i < count; ++i) {
         const fp8act_gemm_problem& p = problems[i];
         if (p.M <= kSkinnyMaxM || p.N == 0) continue;
         const fp8act::GemmProblem g = {static_cast<const uint8_t*>(p.q_e4m3), p.sa,
                                        static_cast<const uint8_t*>(p.w_e4m3), p.sw, p.out, p.M, p.N, p.K};
-        if (p.M > kTileGroupMaxM) {
-            if (int e = one(g)) return e;
-        } else {
-            tiled[n_tiled++] = g;
-        }
+        if (p.M <= kTileGroupMaxM)
+            narrow[n_narrow++] = g;
+        else
+            wide[n_wide++] = g;
     }
     const int cap = fp8act::gemm_tc_grouped_capacity();
-    for (int c0 = 0; c0 < n_tiled; c0 += cap) {
-        const int n = n_tiled - c0 < cap ? n_tiled - c0 : cap;
-        int64_t tiles = 0;
-        for (int j = 0; j < n; ++j) tiles += (tiled[c0 + j].N + 127) / 128;
-        const cudaError_t g =
-            tiles >= sms ? fp8act::launch_gemm_tc_grouped(tiled + c0, n, out_f32, sms, s) : cudaErrorNotSupported;
-        if (g == cudaErrorNotSupported) {  // too few tiles to fill the SMs (or too many to list)
+    auto run_chunks = [&](const fp8act::GemmProblem* list, int n_list, int bn, int64_t min_tiles) -> int {
+        for (int c0 = 0; c0 < n_list; c0 += cap) {
+            const int n = n_list - c0 < cap ? n_list - c0 : cap;
+            int64_t tiles = 0;
             for (int j = 0; j < n; ++j)
-                if (int e = one(tiled[c0 + j])) return e;
-        } else if (int e = launch_status(g)) {
-            return e;
+                tiles += static_cast<int64_t>((list[c0 + j].M + 127) / 128) * ((list[c0 + j].N + bn - 1) / bn);
+            const cudaError_t g = tiles >= min_tiles
+                                      ? fp8act::launch_gemm_tc_grouped(list + c0, n, out_f32, sms, s)
+                                      : cudaErrorNotSupported;
+            if (g == cudaErrorNotSupported) {  // too few tiles to fill the grid (or too many to list)
+                for (int j = 0; j < n; ++j)
+                    if (int e = one(list[c0 + j])) return e;
+            } else if (int e = launch_status(g)) {
+                return e;
+            }
         }
-    }
+        return FP8ACT_OK;
+    };
+    if (int e = run_chunks(narrow, n_narrow, 128, sms)) return e;
+    if (int e = run_chunks(wide, n_wide, 256, 2 * static_cast<int64_t>(sms))) return e;
     return FP8ACT_OK;
 }
 

@@ -568,12 +568,13 @@ struct TcGroupProblem {
     const float* sw;
     void* out;
     int M, N, KB;
+    int mtiles;      // 128-token tiles (walked fastest within a weight column group)
     int tile_begin;  // list position of this problem's first tile
 };
 
 struct TcGroupedArgs {
     CUtensorMap ta[kMaxTcGroup];  // activation codes [M, K], 128 x 128 boxes
-    CUtensorMap tb[kMaxTcGroup];  // weight codes [N, K], 128 x 128 boxes
+    CUtensorMap tb[kMaxTcGroup];  // weight codes [N, K], 128 x BN boxes
     TcGroupProblem p[kMaxTcGroup];
     int count;
     int tiles;                   // list length
@@ -615,13 +616,17 @@ struct GroupedCursor {
             if (t >= 0) p = grouped_problem(a, t);
         }
     }
-    __device__ __forceinline__ int n0(const TcGroupedArgs& a) const { return (t - a.p[p].tile_begin) * 128; }
+    __device__ __forceinline__ int m0(const TcGroupedArgs& a) const {
+        return (t - a.p[p].tile_begin) % a.p[p].mtiles * BM;
+    }
+    __device__ __forceinline__ int n0(const TcGroupedArgs& a, int bn) const {
+        return (t - a.p[p].tile_begin) / a.p[p].mtiles * bn;
+    }
 };
 
-template <bool kF32Out>
-__global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
+template <int BN, bool kF32Out>
+__global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1)
     gemm_tc_grouped_kernel(const __grid_constant__ TcGroupedArgs a) {
-    constexpr int BN = 128;
     using C = TcCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -669,6 +674,9 @@ __global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
 
+    const bool epi = warp >= C::kCtrlWarps;
+    if (!epi) {
+    if constexpr (BN == 256) tc::regs_decrease<C::kRegsCtrl>();
     if (warp == 0) {
         // ------------------------------------------------------- producer
         if (lane == 0) {
@@ -677,8 +685,10 @@ __global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
                 ptx::prefetch_tensormap(&a.ta[p]);
                 ptx::prefetch_tensormap(&a.tb[p]);
             }
-            const uint64_t pol_w = ptx::policy_evict_first();  // every weight tile is read once
-            const uint64_t pol_q = ptx::policy_evict_last();   // a problem's codes are re-read by its tiles
+            // one token tile: every weight tile is read once; several: the token tiles of a
+            // weight column group run together and share it through L2
+            const uint64_t pol_w = BN == 128 ? ptx::policy_evict_first() : ptx::policy_evict_last();
+            const uint64_t pol_q = ptx::policy_evict_last();  // a problem's codes are re-read by its tiles
             const bool skip0 = a.withhold != 0;
             const int pre = total < C::kStages ? total : C::kStages;
             GroupedCursor cw;  // weights: independent of the previous grid
@@ -687,14 +697,15 @@ __global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
                 if (skip0 && i == 0) continue;
                 ptx::mbar_arrive_expect_tx(full0 + 8 * i, C::kStageBytes);
                 ptx::tma_load_2d(base + i * C::kStageBytes + kABytes, &a.tb[cw.p], full0 + 8 * i, cw.kb * kGroup,
-                                 cw.n0(a), pol_w);
+                                 cw.n0(a, BN), pol_w);
             }
             ptx::griddep_wait();  // the activation codes are the previous grid's output
             GroupedCursor ca;
             ca.start(a, b, G);
             for (int i = 0; i < pre; ++i, ca.next(a, b, G)) {
                 if (skip0 && i == 0) continue;
-                ptx::tma_load_2d(base + i * C::kStageBytes, &a.ta[ca.p], full0 + 8 * i, ca.kb * kGroup, 0, pol_q);
+                ptx::tma_load_2d(base + i * C::kStageBytes, &a.ta[ca.p], full0 + 8 * i, ca.kb * kGroup, ca.m0(a),
+                                 pol_q);
             }
             int issued = pre;
             for (int i = pre; i < total; ++i, cw.next(a, b, G)) {
@@ -705,8 +716,9 @@ __global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
                 }
                 ptx::mbar_arrive_expect_tx(full0 + 8 * s, C::kStageBytes);
                 ptx::tma_load_2d(base + s * C::kStageBytes + kABytes, &a.tb[cw.p], full0 + 8 * s, cw.kb * kGroup,
-                                 cw.n0(a), pol_w);
-                ptx::tma_load_2d(base + s * C::kStageBytes, &a.ta[cw.p], full0 + 8 * s, cw.kb * kGroup, 0, pol_q);
+                                 cw.n0(a, BN), pol_w);
+                ptx::tma_load_2d(base + s * C::kStageBytes, &a.ta[cw.p], full0 + 8 * s, cw.kb * kGroup, cw.m0(a),
+                                 pol_q);
                 issued = i + 1;
             }
             // Every copy issued must land before the CTA may leave.
@@ -743,12 +755,14 @@ __global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
             tc::commit(drain);
             if (!ptx::mbar_wait(drain, 0)) fail(abort, 32u);
         }
+    }
     } else {
         // ------------------------------------------------------- epilogue
+        if constexpr (BN == 256) tc::regs_increase<C::kRegsEpi>();
         ptx::griddep_wait();  // scales come from the previous grid; it may still read `out`
         const int qd = warp & 3;                     // TMEM lane quadrant this warp may access
         const int hf = (warp - C::kCtrlWarps) >> 2;  // column half
-        const int row = qd * 32 + lane;              // token
+        const int row = qd * 32 + lane;              // token within the tile
         const uint32_t t_row = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + hf * C::kCols;
         float acc[C::kCols];
         bool failed = false;
@@ -757,13 +771,15 @@ __global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
             const int t = grouped_tile(a, j, b, G);
             if (t < 0) break;
             const TcGroupProblem& pr = a.p[grouped_problem(a, t)];
-            const int n0 = (t - pr.tile_begin) * BN;
+            const int local = t - pr.tile_begin;
+            const int m = local % pr.mtiles * BM + row;
+            const int n0 = local / pr.mtiles * BN;
             const int nb = (n0 + hf * C::kCols) / kGroup;
-            const bool row_ok = row < pr.M && n0 + hf * C::kCols < pr.N;
-            const float* sa_row = pr.sa + static_cast<int64_t>(row_ok ? row : 0) * pr.KB;
+            const bool row_ok = m < pr.M && n0 + hf * C::kCols < pr.N;
+            const float* sa_row = pr.sa + static_cast<int64_t>(row_ok ? m : 0) * pr.KB;
             const float* sw_row = pr.sw + static_cast<int64_t>(row_ok ? nb : 0) * pr.KB;
 #pragma unroll
-            for (int j = 0; j < C::kCols; ++j) acc[j] = 0.f;
+            for (int jj = 0; jj < C::kCols; ++jj) acc[jj] = 0.f;
             for (int k = 0; k < pr.KB; ++k, ++i) {
                 const int acc_b = i & 1;
                 const float scale = row_ok ? ld_dep_f32(sa_row + k) * __ldg(sw_row + k) : 0.f;
@@ -775,50 +791,56 @@ __global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
                     break;
                 }
                 tc::fence_after_sync();
-                uint32_t r0[32], r1[32];
-                tc::ld_32x32b_x32(t_row + acc_b * BN, r0);
-                tc::ld_32x32b_x32(t_row + acc_b * BN + 32, r1);
-                tc::wait_ld();
+                // rounds of 64 columns, both 32-column loads of a round in flight; packed FMAs
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    fma2(acc[j], acc[j + 1], __uint_as_float(r0[j]), __uint_as_float(r0[j + 1]), scale);
-                    fma2(acc[32 + j], acc[33 + j], __uint_as_float(r1[j]), __uint_as_float(r1[j + 1]), scale);
+                for (int c = 0; c < C::kCols / 64; ++c) {
+                    uint32_t r0[32], r1[32];
+                    tc::ld_32x32b_x32(t_row + acc_b * BN + c * 64, r0);
+                    tc::ld_32x32b_x32(t_row + acc_b * BN + c * 64 + 32, r1);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 2) {
+                        fma2(acc[c * 64 + jj], acc[c * 64 + jj + 1], __uint_as_float(r0[jj]),
+                             __uint_as_float(r0[jj + 1]), scale);
+                        fma2(acc[c * 64 + 32 + jj], acc[c * 64 + 33 + jj], __uint_as_float(r1[jj]),
+                             __uint_as_float(r1[jj + 1]), scale);
+                    }
                 }
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(tempty0 + 8 * acc_b);
             }
-            if (row < pr.M && !failed) {
+            if (m < pr.M && !failed) {
                 const int nstart = n0 + hf * C::kCols;
                 if constexpr (kF32Out) {
-                    float* dst = static_cast<float*>(pr.out) + static_cast<int64_t>(row) * pr.N + nstart;
+                    float* dst = static_cast<float*>(pr.out) + static_cast<int64_t>(m) * pr.N + nstart;
                     if ((pr.N & 3) == 0 && nstart + C::kCols <= pr.N) {
 #pragma unroll
-                        for (int j = 0; j < C::kCols; j += 4)
-                            *reinterpret_cast<float4*>(dst + j) =
-                                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                        for (int jj = 0; jj < C::kCols; jj += 4)
+                            *reinterpret_cast<float4*>(dst + jj) =
+                                make_float4(acc[jj], acc[jj + 1], acc[jj + 2], acc[jj + 3]);
                     } else {
 #pragma unroll
-                        for (int j = 0; j < C::kCols; ++j)
-                            if (nstart + j < pr.N) dst[j] = acc[j];
+                        for (int jj = 0; jj < C::kCols; ++jj)
+                            if (nstart + jj < pr.N) dst[jj] = acc[jj];
                     }
                 } else {
                     __nv_bfloat16* dst =
-                        static_cast<__nv_bfloat16*>(pr.out) + static_cast<int64_t>(row) * pr.N + nstart;
+                        static_cast<__nv_bfloat16*>(pr.out) + static_cast<int64_t>(m) * pr.N + nstart;
                     if ((pr.N & 7) == 0 && nstart + C::kCols <= pr.N) {
 #pragma unroll
-                        for (int j = 0; j < C::kCols; j += 8) {
+                        for (int jj = 0; jj < C::kCols; jj += 8) {
                             uint4 v;
-                            v.x = pack_bf16x2(acc[j], acc[j + 1]);
-                            v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-                            v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-                            v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-                            *reinterpret_cast<uint4*>(dst + j) = v;
+                            v.x = pack_bf16x2(acc[jj], acc[jj + 1]);
+                            v.y = pack_bf16x2(acc[jj + 2], acc[jj + 3]);
+                            v.z = pack_bf16x2(acc[jj + 4], acc[jj + 5]);
+                            v.w = pack_bf16x2(acc[jj + 6], acc[jj + 7]);
+                            *reinterpret_cast<uint4*>(dst + jj) = v;
                         }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < C::kCols; ++j)
-                            if (nstart + j < pr.N) dst[j] = __float2bfloat16_rn(acc[j]);
+                        for (int jj = 0; jj < C::kCols; ++jj)
+                            if (nstart + jj < pr.N) dst[jj] = __float2bfloat16_rn(acc[jj]);
                     }
                 }
             }
@@ -831,17 +853,25 @@ __global__ void __launch_bounds__(TcCfg<128>::kThreads, 1)
     if (warp == 1) tc::tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
-template <bool kF32Out>
+template <int BN, bool kF32Out>
 cudaError_t launch_grouped_typed(const TcGroupedArgs& args, int grid, cudaStream_t stream) {
-    using C = TcCfg<128>;
-    auto kernel = gemm_tc_grouped_kernel<kF32Out>;
+    using C = TcCfg<BN>;
+    auto kernel = gemm_tc_grouped_kernel<BN, kF32Out>;
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
+        if constexpr (BN == 256) {
+            // setmaxnreg.inc waits for registers the block does not have if the
+            // compiler allocated fewer than the split assumes: refuse to launch.
+            cudaFuncAttributes fa{};
+            e = cudaFuncGetAttributes(&fa, kernel);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs < C::kRegsLaunch) return cudaErrorInvalidConfiguration;
+        }
         configured.fetch_or(bit, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
@@ -940,6 +970,12 @@ cudaError_t launch_gemm_tc_grouped(const GemmProblem* probs, int count, bool out
                                    cudaStream_t stream) {
     if (count <= 0) return cudaSuccess;
     if (count > kMaxTcGroup) return cudaErrorInvalidValue;
+    // One token tile everywhere (batched decode): 128-wide weight tiles. Otherwise
+    // (prefill widths) 256-wide ones, the token tiles of a column group walked
+    // together, as in the single-problem kernel.
+    bool one_token_tile = true;
+    for (int i = 0; i < count; ++i) one_token_tile = one_token_tile && probs[i].M <= BM;
+    const int bn = one_token_tile ? 128 : 256;
     // problems in order of falling K: a tile's cost is its K groups
     int order[kMaxTcGroup];
     for (int i = 0; i < count; ++i) order[i] = i;
@@ -950,14 +986,14 @@ cudaError_t launch_gemm_tc_grouped(const GemmProblem* probs, int count, bool out
             order[j - 1] = tmp;
         }
     TcGroupedArgs a = {};
-    int tiles = 0;
+    int64_t tiles = 0;
     for (int i = 0; i < count; ++i) {
         const GemmProblem& src = probs[order[i]];
-        if (src.M < 1 || src.M > BM || src.N < 1) return cudaErrorInvalidValue;
+        if (src.M < 1 || src.N < 1) return cudaErrorInvalidValue;
         if (!encode_tmap_2d_u8(&a.ta[i], src.q, static_cast<uint64_t>(src.K), static_cast<uint64_t>(src.M),
                                static_cast<uint64_t>(src.K), kGroup, BM, true) ||
             !encode_tmap_2d_u8(&a.tb[i], src.w, static_cast<uint64_t>(src.K), static_cast<uint64_t>(src.N),
-                               static_cast<uint64_t>(src.K), kGroup, 128, true))
+                               static_cast<uint64_t>(src.K), kGroup, bn, true))
             return cudaErrorInvalidValue;
         TcGroupProblem& d = a.p[i];
         d.sa = src.sa;
@@ -966,26 +1002,25 @@ cudaError_t launch_gemm_tc_grouped(const GemmProblem* probs, int count, bool out
         d.M = src.M;
         d.N = src.N;
         d.KB = src.K / kGroup;
-        d.tile_begin = tiles;
-        tiles += (src.N + 127) / 128;
+        d.mtiles = (src.M + BM - 1) / BM;
+        d.tile_begin = static_cast<int>(tiles);
+        tiles += static_cast<int64_t>(d.mtiles) * ((src.N + bn - 1) / bn);
+        if (tiles > 32767) return cudaErrorNotSupported;  // leftover tiles are recorded as 16-bit positions
     }
-    if (tiles > 32767) return cudaErrorNotSupported;  // leftover tiles are recorded as 16-bit positions
     a.count = count;
-    a.tiles = tiles;
+    a.tiles = static_cast<int>(tiles);
     a.wait_ns = tile_wait_limit_ns();
     a.withhold = tile_withhold_first_load() ? 1 : 0;
-    int grid = tiles < num_sms ? tiles : num_sms;
+    int grid = a.tiles < num_sms ? a.tiles : num_sms;
     if (grid > kMaxTcGroupCtas) grid = kMaxTcGroupCtas;
     // Whole snake rounds, then the partial round's tiles (largest first) to
     // the CTAs with the fewest K groups after the whole rounds.
-    a.full_rounds = tiles / grid;
-    const int partial = tiles - a.full_rounds * grid;
-    int kb_of[kMaxTcGroup + 1];
-    for (int i = 0; i < count; ++i) kb_of[i] = a.p[i].KB;
+    a.full_rounds = a.tiles / grid;
+    const int partial = a.tiles - a.full_rounds * grid;
     auto cost = [&](int t) {
         int i = 0;
         while (i + 1 < count && t >= a.p[i + 1].tile_begin) ++i;
-        return kb_of[i];
+        return a.p[i].KB;
     };
     int load[kMaxTcGroupCtas], by_load[kMaxTcGroupCtas];
     for (int c = 0; c < grid; ++c) {
@@ -996,7 +1031,10 @@ cudaError_t launch_gemm_tc_grouped(const GemmProblem* probs, int count, bool out
     }
     std::stable_sort(by_load, by_load + grid, [&](int x, int y) { return load[x] < load[y]; });
     for (int i = 0; i < partial; ++i) a.leftover[by_load[i]] = static_cast<short>(a.full_rounds * grid + i);
-    return out_f32 ? launch_grouped_typed<true>(a, grid, stream) : launch_grouped_typed<false>(a, grid, stream);
+    if (bn == 128)
+        return out_f32 ? launch_grouped_typed<128, true>(a, grid, stream)
+                       : launch_grouped_typed<128, false>(a, grid, stream);
+    return out_f32 ? launch_grouped_typed<256, true>(a, grid, stream) : launch_grouped_typed<256, false>(a, grid, stream);
 }
 
 }  // namespace fp8act

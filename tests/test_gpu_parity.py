@@ -381,6 +381,44 @@ def test_gemm_grouped_every_route_in_one_call(fp8act):
     _grouped_compare(fp8act, probs, [m for _, _, m in dims], seed=995)
 
 
+def test_gemm_grouped_prefill_five_shapes(fp8act):
+    """Prefill width (M = 4096) over the five projections in one grouped call:
+    5376 tiles of 128 tokens x 256 weight rows in one persistent launch (the
+    token tiles of a column group together, the tiles dealt over the CTAs in
+    order of falling K). Every output column of about 640 rows per shape (the
+    prefill test's rows: first and last 128, one per token tile and TMEM lane
+    quadrant, 256 random) against the oracle; on the three shapes whose own
+    call has no split tail, all outputs equal that call's bit for bit."""
+    from parity_util import compare_gemm, oracle_gemm, tile_rows
+    ps = [problem(si) for si in range(len(SHAPES))]
+    acts = [p.activations(4096, 1300 + i) for i, p in enumerate(ps)]
+    args = [(q, sa, p.w, p.sw) for (q, sa, _, _), p in zip(acts, ps)]
+    outs = fp8act.fp8_block_gemm_grouped(args)
+    outs32 = fp8act.fp8_block_gemm_grouped_f32(args)
+    torch.cuda.synchronize()
+    for si, ((q, sa, q_ref, sa_ref), p, o, o32) in enumerate(zip(acts, ps, outs, outs32)):
+        rows = tile_rows(4096, 256, seed=1310 + si)
+        y, aabs, ref = oracle_gemm(q_ref, sa_ref, p.w_ref, p.sw_ref, rows=rows)
+        idx = torch.as_tensor(np.asarray(rows), device=o.device)
+        compare_gemm(o.index_select(0, idx), o32.index_select(0, idx), y, aabs, ref, p.K)
+        if p.N != 5120:  # (5120, K) runs a split tail of its own
+            single = fp8act.fp8_block_gemm_f32(q, sa, p.w, p.sw)
+            torch.cuda.synchronize()
+            assert torch.equal(o32, single), (p.N, p.K)
+
+
+def test_gemm_grouped_wide_ragged(fp8act):
+    """The grouped 256-wide launch on ragged problems: M from 129 to 1000 (a
+    last token tile of 1 .. 127 rows), N ending inside a 256-wide tile and a
+    scale block, K from 2 to 8 groups, 323 tiles (past two waves, so the
+    grouped launch is taken); every output against the oracle."""
+    from parity_util import Problem
+    dims = [(5000, 512, 1000), (3000, 640, 300), (9000, 256, 129), (2600, 1024, 600)]
+    assert sum(((m + 127) // 128) * ((N + 255) // 256) for N, _, m in dims) >= 304
+    probs = [Problem(N, K, seed=1400 + i) for i, (N, K, _) in enumerate(dims)]
+    _grouped_compare(fp8act, probs, [m for _, _, m in dims], seed=1410)
+
+
 def test_gemm_grouped_batched_equals_single_call_without_split(fp8act):
     """(17408, 5120) alone runs 136 unsplit tiles, one K order per tile; in a
     grouped launch with the other projections each of its tiles runs the
