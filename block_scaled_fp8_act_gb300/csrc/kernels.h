@@ -54,11 +54,12 @@ struct GemmProblem {
 // weight-streaming kernel (each CTA finds its problem from its index).
 cudaError_t launch_gemm_skinny_grouped(const GemmProblem* probs, int count, bool out_f32, cudaStream_t stream);
 
-// Several batched-decode problems (16 < M <= 128 each, one token tile) in
-// one persistent launch of the 128 x 128 tile kernel: all their weight tiles
-// in one list dealt evenly over the CTAs, K never split. At most
-// gemm_tc_grouped_capacity() problems per launch; worth it when their tiles
-// fill the SMs. cudaErrorNotSupported (nothing launched) past 32767 tiles.
+// Several problems (M > 16) in one persistent launch of the tcgen05 tile
+// kernel: 128 x 128 tiles when every M <= 128 (one token tile each), 128 x
+// 256 tiles otherwise; all their tiles in one list dealt evenly over the
+// CTAs, K never split. At most gemm_tc_grouped_capacity() problems per
+// launch; worth it when their tiles fill the SMs (two waves for 256-wide
+// ones). cudaErrorNotSupported (nothing launched) past 32767 tiles.
 int gemm_tc_grouped_capacity();
 cudaError_t launch_gemm_tc_grouped(const GemmProblem* probs, int count, bool out_f32, int num_sms,
                                    cudaStream_t stream);

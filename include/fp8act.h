@@ -220,9 +220,11 @@ FP8ACT_API int fp8_act_quant_grouped(const fp8act_quant_problem* problems, int c
  * share one launch of the weight-streaming kernel (largest weights first).
  * Those with 16 < M <= 128 share one persistent launch of the tcgen05 tile
  * kernel per 8 problems when their 128-row weight tiles at least fill the
- * SMs (the tiles of all problems dealt evenly over the CTAs, K never split);
- * otherwise, and for M > 128, one tile-kernel launch each. All on the same
- * stream; the results equal fp8_block_gemm's within its tolerance.
+ * SMs, those with M > 128 one per 8 problems when their 256-row tiles fill
+ * two waves (the tiles of all problems dealt evenly over the CTAs, K never
+ * split); a chunk with fewer tiles runs one tile-kernel launch per problem.
+ * All on the same stream; the results equal fp8_block_gemm's within its
+ * tolerance.
  */
 FP8ACT_API int fp8_block_gemm_grouped(const fp8act_gemm_problem* problems, int count, void* stream);
 FP8ACT_API int fp8_block_gemm_grouped_f32(const fp8act_gemm_problem* problems, int count, void* stream);
