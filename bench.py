@@ -549,8 +549,8 @@ def sweep(weights, device, stream, peaks) -> dict:
     """us/call of the block GEMM per shape at every workload M (outside the
     timed step), compact: per M the five us/call and the fraction of the
     roofline (HBM up to M = 102, FP8 tensor peak at 4096; burst peaks, each
-    GEMM runs alone); and at M = 64 and 102 the five shapes as one grouped
-    call (one launch)."""
+    GEMM runs alone); and at M = 64, 102 and 4096 the five shapes as one
+    grouped call (one launch)."""
     res = {"shapes": [list(sh) for sh in weights.shapes], "us": {}, "frac": {}}
     hbm = peaks["hbm_gbs"]
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
@@ -565,13 +565,16 @@ def sweep(weights, device, stream, peaks) -> dict:
         res["frac"][str(M)] = [round(f, 3) for f in fr]
         del wl
         torch.cuda.empty_cache()
-    # the five shapes as one grouped call at the batched widths (one launch: us and fraction of the lot)
+    # the five shapes as one grouped call (one launch: us and fraction of the lot)
     res["grouped"] = {}
-    for M in (64, 102):
+    for M in (64, 102, 4096):
         wl = Workload(M, weights, device, grouped=True)
-        (t,) = gemm_kernel_times(wl, stream, launches=30, reps=3)
-        b = sum(algorithmic_gemm_bytes(M, N, K) for N, K in wl.shapes)
-        res["grouped"][str(M)] = {"us": round(t * 1e6, 2), "frac": round(b / t / 1e9 / hbm, 3)}
+        (t,) = gemm_kernel_times(wl, stream, launches=30 if M <= 102 else 3, reps=3)
+        if M <= 102:
+            fr = sum(algorithmic_gemm_bytes(M, N, K) for N, K in wl.shapes) / t / 1e9 / hbm
+        else:
+            fr = sum(2.0 * M * N * K for N, K in wl.shapes) / t / 1e12 / fp8_peak
+        res["grouped"][str(M)] = {"us": round(t * 1e6, 2), "frac": round(fr, 3)}
         del wl
         torch.cuda.empty_cache()
     return res
