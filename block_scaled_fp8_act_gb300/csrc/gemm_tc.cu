@@ -35,9 +35,13 @@
 // N = 5120 projections has 40 tiles of 128 rows), a cluster of S CTAs shares
 // a tile, each taking a contiguous slice of the K groups. At the end every CTA
 // parks its fp32 partial tile in its own (now idle) stage memory, the cluster
-// synchronises once, and CTA r adds rows [128 r / S, 128 (r + 1) / S) of all S
-// partials through distributed shared memory, in rank order (deterministic),
-// and stores them. No global scratch, no atomics.
+// synchronises once, and CTA r adds its share of the tile's real token rows
+// of all S partials through distributed shared memory, in rank order
+// (deterministic), and stores them. No global scratch, no atomics.
+//
+// Grouped calls (gemm_tc_grouped_kernel, further down): the tiles of up to 8
+// problems in one persistent launch, dealt evenly over the CTAs, K never
+// split.
 //
 // Failure handling: every wait is bounded (the bound is a launch argument).
 // The first wait that gives up sets the device error word read by
@@ -546,20 +550,24 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, const TcA
 }
 
 // ------------------------------------------------------------------------
-// Grouped batched decode: several problems of one token tile each
-// (16 < M <= 128) in one persistent launch of the 128 x 128 tile kernel.
-// The problems' weight tiles form one list, problems in order of falling K
-// (a tile costs its K groups). With G CTAs the list runs in whole rounds of
+// Grouped calls: several problems in one persistent launch of the tile
+// kernel. BN = 128 when every problem has one token tile (16 < M <= 128,
+// batched decode), BN = 256 otherwise (prefill widths, with the 12-warp
+// register split of gemm_tc_kernel<256>); a problem's token tiles are walked
+// fastest within a weight column group, so a wave shares its weight tiles
+// through L2. The problems' tiles form one list, problems in order of falling
+// K (a tile costs its K groups). With G CTAs the list runs in whole rounds of
 // G tiles, CTA b taking position r G + b in even rounds r and r G + G - 1 - b
 // in odd ones (a snake, so the costly first tiles spread over all CTAs); the
 // tiles of the last, partial round go, largest first, to the CTAs with the
 // fewest K groups so far (the host works that out; the kernel gets each
-// CTA's leftover tile). The tiles of several projections fill the grid without splitting
-// K, so there is no cross-CTA reduction (on one N = 5120 projection alone
-// that reduction is a third of the launch), and the stage ring and the two
-// accumulators run on across the tiles of different problems. Each problem
-// has its own tensor maps in the kernel parameters. Roles, barriers, bounded
-// waits and the drain are those of gemm_tc_kernel.
+// CTA's leftover tile). The tiles of several projections fill the grid
+// without splitting K, so there is no cross-CTA reduction (on one N = 5120
+// projection alone at batched widths that reduction is a third of the
+// launch) and no last partial wave per problem, and the stage ring and the
+// two accumulators run on across the tiles of different problems. Each
+// problem has its own tensor maps in the kernel parameters. Roles, barriers,
+// bounded waits and the drain are those of gemm_tc_kernel.
 constexpr int kMaxTcGroup = 8;        // problems per launch (their tensor maps travel in the parameters)
 constexpr int kMaxTcGroupCtas = 256;  // grid limit of the grouped launch
 
