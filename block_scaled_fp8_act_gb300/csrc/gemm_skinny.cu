@@ -718,9 +718,7 @@ __global__ void __launch_bounds__(pq_max_warps<kUnroll>() * 32, 1) linear_persis
     // i % (2 nwarps), so every warp shares the work, and a slot's groups of
     // one pass (pq_quant_unroll) have their loads issued together.
     auto prologue = [&]() {
-        ptx::griddep_wait();
         const int rank = csize > 1 ? static_cast<int>(ptx::cluster_ctarank()) : 0;
-        if (csize > 1) ptx::cluster_wait();  // every peer has started
         const int half = lane >> 4, hl = lane & 15;
         const int ngroups = a.M * a.KB;
         const int mine = (ngroups - rank + csize - 1) / csize;  // groups rank, rank + C, ... < ngroups
@@ -728,6 +726,22 @@ __global__ void __launch_bounds__(pq_max_warps<kUnroll>() * 32, 1) linear_persis
         const int slot = 2 * warp + half;
         const uint4 zero = make_uint4(0, 0, 0, 0);
         constexpr int kQU = pq_quant_unroll<kUnroll>();
+        // The x lines of the slot's first pass go to L2 before the wait (a
+        // cache hint only: the previous grid's writes land in L2, so the
+        // loads after the wait still see them), which takes the DRAM round
+        // trip of an x that has left L2 off the start of the weight stream.
+        if ((hl & 7) == 0) {
+#pragma unroll
+            for (int u = 0; u < kQU; ++u) {
+                const int li = u * slots + slot;
+                if (li < mine) {
+                    const int gi = rank + li * csize;
+                    prefetch_l2(a.x + (static_cast<int64_t>(gi / a.KB) * a.K + (gi % a.KB) * kGroup + 8 * hl) * 2);
+                }
+            }
+        }
+        ptx::griddep_wait();
+        if (csize > 1) ptx::cluster_wait();  // every peer has started
         for (int base = 0; base < mine; base += kQU * slots) {
             uint4 v[kQU];
 #pragma unroll

@@ -94,8 +94,25 @@ __device__ __forceinline__ void act_quant_body(const Map& map, int64_t groups, i
 
     // Programmatic dependent launch: let the next kernel (the GEMM, whose
     // weight stream does not depend on us) start launching now, then wait for
-    // the grid that produced x (and may still read q / sa) to finish.
+    // the grid that produced x (and may still read q / sa) to finish. Before
+    // the wait, the two 128-byte lines of each of this warp's first groups
+    // are prefetched to L2. A prefetch is only a cache hint and L2 is where
+    // the previous grid's writes land, so the loads after the wait still see
+    // them; what it saves is the DRAM round trip of an x that has left L2.
     ptx::griddep_launch_dependents();
+    if ((hl & 7) == 0) {
+#pragma unroll
+        for (int u = 0; u < kActUnroll; ++u) {
+            const int64_t g = warp * per_iter + 2 * u + half;
+            if (g < groups) {
+                const uint4* xg;
+                uint2* qg;
+                float* sg;
+                map.at(g, xg, qg, sg);
+                prefetch_l2(xg + hl);
+            }
+        }
+    }
     ptx::griddep_wait();
     uint4 v[kActUnroll];
     load(warp * per_iter, v);
