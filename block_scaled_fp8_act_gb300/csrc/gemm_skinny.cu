@@ -783,7 +783,9 @@ __global__ void __launch_bounds__(pq_max_warps<kUnroll>() * 32, 1) linear_persis
             __syncthreads();
     };
     float(*const red)[16][8] = red_all + group * a.wg;
-    const int first = blockIdx.x * a.groups + group;
+    // tiles dealt round-robin over the CTAs, then the groups: tile t runs on
+    // CTA t % gridDim.x, so every SM of the grid streams
+    const int first = blockIdx.x + group * gridDim.x;
     // Depth 4 (short K): the first tile issues its first weight loads (four
     // K blocks per warp) before the prologue, as the two-launch kernel does
     // before its wait. Depth 1: the first tile's lines are only prefetched to
@@ -1028,8 +1030,8 @@ cudaError_t launch_persistent_typed(const void* x, const uint8_t* w, const float
     a.groups = groups;
     const size_t smem = pq_smem_bytes(M, K, groups, wv);
     if (smem > 227 * 1024) return cudaErrorNotSupported;
-    const int64_t want = (static_cast<int64_t>(a.tiles) + groups - 1) / groups;
-    int grid = static_cast<int>(want < num_sms ? want : num_sms);
+    // one CTA per SM (or per tile, if fewer), each taking every grid-th tile
+    int grid = a.tiles < num_sms ? a.tiles : num_sms;
     // Share the quantisation over a cluster when each SM would otherwise
     // quantise many groups. The grid becomes whole clusters, all resident at
     // once (CTAs past the last tile only quantise their share): rounded up,
