@@ -110,29 +110,6 @@ struct MidArgs {
     int table_bytes;  // shared memory of the scale table (multiple of 16)
 };
 
-// Four consecutive outputs out[o .. o + 3], of which `room` (may be < 4) lie
-// inside the row; one vector store when the row allows it.
-template <bool kF32Out>
-__device__ __forceinline__ void store4(void* out, int64_t o, int room, bool vec_ok, const float4& v) {
-    if (vec_ok && room >= 4) {
-        if constexpr (kF32Out)
-            *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = v;
-        else
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + o) =
-                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-        return;
-    }
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        if (t >= room) break;
-        if constexpr (kF32Out)
-            static_cast<float*>(out)[o + t] = vv[t];
-        else
-            static_cast<__nv_bfloat16*>(out)[o + t] = __float2bfloat16_rn(vv[t]);
-    }
-}
-
 __device__ __forceinline__ void fail(volatile int* abort, unsigned int code) {
     *abort = 1;
     atomicOr(&g_midm_error, code);

@@ -137,23 +137,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Named barrier over `threads` threads that also ORs a predicate across
-// them: every participant gets the same answer (a uniform decision).
-__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n"
-        ".reg .pred p, q;\n"
-        "setp.ne.u32 p, %3, 0;\n"
-        "barrier.cta.red.or.pred q, %1, %2, p;\n"
-        "selp.u32 %0, 1, 0, q;\n"
-        "}\n"
-        : "=r"(r)
-        : "r"(id), "r"(threads), "r"(static_cast<uint32_t>(pred))
-        : "memory");
-    return r != 0;
-}
-
 // Thread-block clusters: rank of this CTA, cluster-wide barrier (every
 // thread of every CTA in the cluster arrives; release / acquire ordering of
 // shared memory), and loads from a peer CTA's shared memory.
@@ -179,11 +162,6 @@ __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
 // Stores into a (possibly peer) CTA's shared memory at a mapa_shared address.
 __device__ __forceinline__ void st_shared_cluster_v2(uint32_t addr, uint2 v) {
     asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
@@ -200,41 +178,13 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
-// Bulk (non-tensor) copies through the TMA engine. Addresses 16-byte aligned,
-// sizes a multiple of 16 bytes.
-__device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every committed bulk group of this thread has completed (its writes performed).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Bulk (non-tensor) copy through the TMA engine, global -> shared, completing
+// `bytes` of transaction count on `bar`. Addresses 16-byte aligned, size a
+// multiple of 16 bytes.
 __device__ __forceinline__ void bulk_load_g2s(uint32_t sdst, const void* gsrc, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
                  "l"(gsrc), "r"(bytes), "r"(bar)
                  : "memory");
 }
-// Order generic-proxy accesses to shared / global memory against async-proxy (TMA) ones.
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
-// 4-byte asynchronous global -> shared copy (L1 path); src_bytes = 0 writes
-// zero and reads nothing. Completion: cp_async_commit / cp_async_wait.
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most kPending of this thread's committed groups are still in flight.
-template <int kPending>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
-}
-
-__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-
 }  // namespace ptx
 }  // namespace fp8act
