@@ -306,6 +306,19 @@ def test_vocab_head_w8a16(fp8act, vocab_problem):
     _w8a16_compare(fp8act, vocab_problem, 1, seed=711)
 
 
+@pytest.mark.parametrize("M", [1, 8])
+def test_vocab_head_fused(fp8act, vocab_problem, M):
+    """`fp8_linear` on the vocabulary head: 9496 tiles dealt over one CTA per
+    SM, so every warp group walks several rounds of tiles (M = 8 also shares
+    the quantisation over 4-CTA clusters). Oracle parity, and the fp32 result
+    equals the two-launch path's bit for bit."""
+    xd, out32 = _linear_compare(fp8act, vocab_problem, M, seed=720 + M)
+    q, sa = fp8act.fp8_act_quant(xd)
+    ref32 = fp8act.fp8_block_gemm_f32(q, sa, vocab_problem.w, vocab_problem.sw)
+    torch.cuda.synchronize()
+    assert torch.equal(out32, ref32)
+
+
 # ------------------------------------------------------------ grouped calls
 def test_act_quant_grouped_bit_exact(fp8act):
     """One launch over the five K's and ragged M's, bit-exact per problem."""
