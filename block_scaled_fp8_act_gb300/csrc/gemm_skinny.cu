@@ -53,10 +53,12 @@
 // weight loads are in flight: no warp waits for another. Every CTA repeats
 // the quantisation of the same tokens.
 //
-// Fused, one quantisation per SM (linear_persistent_kernel, M <= 8): one CTA
+// Fused, one quantisation per SM (linear_persistent_kernel, M <= 16): one CTA
 // per SM whose warps quantise all the tokens once into shared memory and
-// then, in groups, stream the weight tiles with this file's loop and the
-// two-launch path's warp count per tile (so the same sums); it replaces the
+// then, in groups, stream the weight tiles (16 rows x 8 tokens; above 8
+// tokens each row tile twice, the second read mostly from L2, as the
+// two-launch grid does) with this file's loop and the two-launch path's
+// warp count per tile (so the same sums); it replaces the
 // per-CTA quantisation, which a timeline trace showed stalling every CTA's
 // weight stream for several microseconds. From two tokens on, a
 // thread-block cluster of 2 or 4 CTAs shares the quantisation: each CTA
@@ -535,10 +537,10 @@ cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, co
 }
 
 // ------------------------------------------------------------------------
-// Fused mode with one quantisation per SM (M <= 8). One CTA per SM, up to 32
-// warps in groups of `wg`; each group takes the weight tiles
-// blockIdx.x * groups + group, + gridDim.x * groups, ... and runs the
-// two-launch kernel's loop on each (the same warp count per tile, so the
+// Fused mode with one quantisation per SM (M <= 16). One CTA per SM, up to 32
+// warps in groups of `wg`; tile t (16 weight rows x 8 tokens) runs on CTA
+// t % gridDim.x, group (t / gridDim.x) % groups, and each group runs the
+// two-launch kernel's loop on its tiles (the same warp count per tile, so the
 // same K order and sums), reading the activation codes and scales from
 // shared memory, where the CTA's warps (or, with a cluster, the cluster's
 // CTAs) put them once, after the programmatic-launch wait, with the
@@ -575,6 +577,7 @@ struct PqArgs {
     const float* sw;
     void* out;
     int M, N, K, KB, tiles;
+    int tg;       // groups of 8 tokens (1 or 2); tile t = weight rows 16 (t / tg), tokens 8 (t % tg)
     int wg;       // warps per tile
     int groups;   // warp groups per CTA
     int cluster;  // CTAs per thread-block cluster sharing the quantisation (1, 2, 4 or 8)
@@ -587,16 +590,17 @@ inline size_t pq_smem_bytes(int M, int K, int groups, int wg) {
     return static_cast<size_t>(pq_red_offset(M, K, K / kGroup)) + static_cast<size_t>(groups) * wg * 16 * 8 * 4;
 }
 
-// One 16-row tile by the warps of one group: the W8A8 loop of skinny_tile
-// (same load depth, K permutation, MMA order, scale products and warp-order
-// sum), with the codes and scales read from shared memory.
+// One tile (16 weight rows x 8 tokens) by the warps of one group: the W8A8
+// loop of skinny_tile (same load depth, K permutation, MMA order, scale
+// products and warp-order sum), with the codes and scales read from shared
+// memory.
 template <bool kF32Out, int kUnroll, bool kWide, class Prologue>
 __device__ __forceinline__ void pq_tile(const PqArgs& a, const uint8_t* __restrict__ q_s, const float* __restrict__ sa_s,
                                         float (*red)[16][8], int tile, int gw, uint32_t bar_id, bool run_prologue,
                                         const Prologue& prologue) {
     const int KB = a.KB, K = a.K, M = a.M, N = a.N, wg = a.wg;
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int n0 = tile * 16;
+    const int n0 = (tile / a.tg) * 16, m0 = (tile % a.tg) * 8;
     const bool ok_r0 = n0 + g < N, ok_r1 = n0 + g + 8 < N;
     const int lane_off = kWide ? 32 * t : 16 * t;
     constexpr int kHiOff = kWide ? 16 : 64;
@@ -615,9 +619,9 @@ __device__ __forceinline__ void pq_tile(const PqArgs& a, const uint8_t* __restri
                 if (kb < KB) prefetch_l2(w_pf + static_cast<int64_t>(kb) * kGroup);
             }
     }
-    const bool ok_x = g < M;
-    const uint8_t* x_r = q_s + g * pq_codes_stride(K) + lane_off;
-    const int c0 = 2 * t;
+    const bool ok_x = m0 + g < M;
+    const uint8_t* x_r = q_s + (m0 + g) * pq_codes_stride(K) + lane_off;
+    const int c0 = m0 + 2 * t;  // token columns of this lane's accumulators: c0, c0 + 1
     const uint4 zero = make_uint4(0, 0, 0, 0);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int kb0 = gw; kb0 < KB; kb0 += stride) {
@@ -682,8 +686,8 @@ __device__ __forceinline__ void pq_tile(const PqArgs& a, const uint8_t* __restri
         float v = 0.f;
         for (int ww = 0; ww < wg; ++ww) v += red[ww][r][c];
         const int n = n0 + r;
-        if (n < N && c < M) {
-            const int64_t o = static_cast<int64_t>(c) * N + n;
+        if (n < N && m0 + c < M) {
+            const int64_t o = static_cast<int64_t>(m0 + c) * N + n;
             if constexpr (kF32Out)
                 static_cast<float*>(a.out)[o] = v;
             else
@@ -793,8 +797,8 @@ __global__ void __launch_bounds__(pq_max_warps<kUnroll>() * 32, 1) linear_persis
     // there (64 registers: the prologue's own registers crowd them).
     constexpr bool kLoadsFirst = kUnroll > 1;
     if (!kLoadsFirst || first >= a.tiles) {  // a group without tiles still takes part in the prologue
-        if (!kLoadsFirst && first < a.tiles && lane < 16 && first * 16 + lane < a.N) {
-            const uint8_t* w_pf = a.w + static_cast<int64_t>(first * 16 + lane) * a.K;
+        if (!kLoadsFirst && first < a.tiles && lane < 16 && (first / a.tg) * 16 + lane < a.N) {
+            const uint8_t* w_pf = a.w + static_cast<int64_t>((first / a.tg) * 16 + lane) * a.K;
 #pragma unroll
             for (int st = 0; st <= kL2Ahead; ++st) {
                 const int kb = gw + st * a.wg;
@@ -1002,7 +1006,7 @@ bool fused_fits(int M, int K) {
 
 namespace {
 
-// The fused kernel with one quantisation per SM, M <= 8; cudaErrorNotSupported
+// The fused kernel with one quantisation per SM, M <= 16; cudaErrorNotSupported
 // (nothing launched) when the codes do not fit shared memory.
 template <bool kF32Out, int kUnroll, bool kWide>
 cudaError_t launch_persistent_typed(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
@@ -1016,8 +1020,12 @@ cudaError_t launch_persistent_typed(const void* x, const uint8_t* w, const float
     a.N = N;
     a.K = K;
     a.KB = K / kGroup;
-    a.tiles = (N + 15) / 16;
-    // warps per tile: the two-launch kernel's choice for this shape (same K order, same sums)
+    // tiles of 16 weight rows x 8 tokens, the token groups of one row tile
+    // adjacent (neighbouring CTAs, so the second read of the rows hits L2)
+    a.tg = (M + 7) / 8;
+    a.tiles = (N + 15) / 16 * a.tg;
+    // warps per tile: the two-launch kernel's choice for this shape, whose
+    // grid has as many CTAs as these tiles (same K order, same sums)
     constexpr int kMode = kWide ? (kModeW8A8 | kWideBit) : kModeW8A8;
     int wv = pick_warps<kF32Out, kUnroll, 1, kMode>(a.tiles, a.KB, num_sms, nullptr, M);
     if (wv == 0) wv = a.KB < 4 ? a.KB : 4;
@@ -1065,7 +1073,7 @@ cudaError_t launch_persistent_any(const void* x, const uint8_t* w, const float* 
 
 cudaError_t launch_linear_fused(const void* x, const uint8_t* w, const float* sw, int M, int N, int K, void* out,
                                 bool out_f32, int num_sms, cudaStream_t stream) {
-    if (M <= 8) {
+    if (M <= 16) {
         const cudaError_t e = out_f32 ? launch_persistent_any<true>(x, w, sw, M, N, K, out, num_sms, stream)
                                       : launch_persistent_any<false>(x, w, sw, M, N, K, out, num_sms, stream);
         if (e != cudaErrorNotSupported) return e;

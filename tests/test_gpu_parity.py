@@ -466,14 +466,15 @@ def test_linear_fused_decode_widths(fp8act, si, M):
 
 
 @pytest.mark.parametrize("si", range(len(SHAPES)))
-@pytest.mark.parametrize("M", [1, 2, 5, 8])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 12, 16])
 def test_linear_fused_equals_two_launches(fp8act, si, M):
-    """For M <= 8 the fused kernel runs the two-launch path's warp count per
+    """For M <= 16 the fused kernel runs the two-launch path's warp count per
     tile and its loop, so equal codes and scales give the same fp32 sums bit
     for bit: any code or scale the in-kernel quantisation got wrong would
     show here. M = 1 quantises per SM; M = 2, 5, 8 on these shapes share the
     quantisation over clusters of 2 or 4 CTAs (each CTA writes its share into
-    every peer's shared memory)."""
+    every peer's shared memory); M = 12, 16 add a second 8-token group per
+    weight tile."""
     p = problem(si)
     xd, out32 = _linear_compare(fp8act, p, M, seed=650 + 10 * M + si)
     q, sa = fp8act.fp8_act_quant(xd)
