@@ -151,18 +151,20 @@ FP8ACT_API int fp8_block_gemm_w8a16_f32(const void* x_bf16, const void* w_e4m3, 
  * counts the quantisation launch per linear layer among the costs of the
  * W8A8 path at one request, and the zskr.cn Qwen3-27B decode article,
  * section 3.3, fuses the quantisation op into the preceding computation.
- * For M <= 8 one CTA per SM quantises all the tokens once into shared
+ * For M <= 16 one CTA per SM quantises all the tokens once into shared
  * memory after the wait for the previous kernel (from M = 2 on, a
  * thread-block cluster of 2 or 4 CTAs splits that work and each CTA stores
- * its groups into every peer's shared memory), then its warp
- * groups stream the weight tiles with the two-launch kernel's loop (the same
- * sums: at M = 1 the result equals the two-launch path bit for bit). Above
- * M = 8, or where the codes do not fit shared memory, every warp of the
+ * its groups into every peer's shared memory), then its warp groups stream
+ * the weight tiles (16 rows x 8 tokens) with the two-launch kernel's loop
+ * and warp count (the same sums: the result equals the two-launch path bit
+ * for bit). Above M = 16, or where the M x K codes do not fit the CTA's
+ * shared memory (about K <= 13000 at 16 tokens), every warp of the
  * weight-streaming kernel quantises the 1x128 groups of the K blocks it
- * multiplies (for its at most 8 tokens) into shared memory. Each SM (or
- * cluster, or CTA) repeats the activation work, so the call is meant for
- * one-token decode: there it is about level with the two launches, and it
- * is slower from M = 2 on (by ~12% at M = 8). The codes and scales of min(8, M)
+ * multiplies (for its at most 8 tokens) into shared memory, which repeats
+ * the activation work in every CTA and is several times slower. The call is
+ * meant for decode and speculative verify: on the five projection shapes it
+ * is ~5% faster than the two launches at one token, level at 4 and 9
+ * tokens, and 7-8% slower at 8 and 16. The codes and scales of min(8, M)
  * tokens take min(8, M) * K * 33 / 32 bytes of shared memory per CTA in the
  * per-warp kernel, at most 200 KiB (K <= 24576 once M >= 8); larger K
  * returns FP8ACT_ERR_SHAPE.
