@@ -390,8 +390,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) gemm_skinny_kernel(
     const float* __restrict__ sw, int M, int N, int K, void* __restrict__ out) {
     __shared__ float red[kMaxWarps][16][8 * kTG];
     extern __shared__ __align__(16) uint8_t fq_smem[];
-    skinny_tile<kF32Out, kUnroll, kTG, kMode>(q, sa, w, sw, M, N, K, out, blockIdx.x * 16, blockIdx.y * 8 * kTG,
-                                              red, fq_smem);
+    // CTA b: token group b % ty of weight-row tile b / ty (the token groups of
+    // one row tile on adjacent CTAs, so the rows' second read hits L2)
+    const int ty = (M + 8 * kTG - 1) / (8 * kTG);
+    skinny_tile<kF32Out, kUnroll, kTG, kMode>(q, sa, w, sw, M, N, K, out, (blockIdx.x / ty) * 16,
+                                              (blockIdx.x % ty) * 8 * kTG, red, fq_smem);
 }
 
 // Several independent problems in one grid: CTA b belongs to the problem p
@@ -502,8 +505,9 @@ template <bool kF32Out, int kUnroll, int kTG, int kMode = kModeW8A8>
 cudaError_t launch_typed(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M, int N, int K,
                          void* out, int num_sms, cudaStream_t stream) {
     const int KB = K / kGroup;
-    const dim3 grid((N + 15) / 16, (M + 8 * kTG - 1) / (8 * kTG));
-    const int64_t ctas = static_cast<int64_t>(grid.x) * grid.y;
+    const int64_t ctas = static_cast<int64_t>((N + 15) / 16) * ((M + 8 * kTG - 1) / (8 * kTG));
+    if (ctas > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(ctas));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     // The fused mode gives each warp a slice of dynamic shared memory.
