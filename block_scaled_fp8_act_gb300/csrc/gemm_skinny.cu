@@ -896,8 +896,9 @@ cudaError_t launch_persistent(const PqArgs& a, int grid, size_t smem, cudaStream
 cudaError_t launch_gemm_skinny_unroll(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
                                       int N, int K, void* out, bool out_f32, int num_sms, int unroll,
                                       cudaStream_t stream) {
-    // Above M = 8 the grid gets one row of CTAs per 8 tokens (each re-reads
-    // the weights, mostly from L2); for 9..16 tokens this measured faster than
+    // Above M = 8 the grid gets a CTA per 8 tokens and row tile, the token
+    // groups of a row tile on adjacent CTAs (each re-reads the weights, the
+    // second read mostly from L2); for 9..16 tokens this measured faster than
     // CTAs that hold 16 tokens against one weight fragment.
     // 256-bit weight and code loads on the depth-4 (short K) path when both
     // start on 32-byte boundaries (rows are K bytes apart, K a multiple of

@@ -26,8 +26,8 @@ cudaError_t launch_weight_quant(const void* W, int64_t N, int64_t K, void* w, fl
 
 // Weight-streaming GEMM for small M (tensor-core mma.sync, 16-row tiles,
 // K split across the warps of a CTA, programmatic dependent launch). Any M
-// works (one row of CTAs per 8 tokens) but every row re-reads the weights,
-// so it is the M <= 16 path.
+// works (a CTA per 8 tokens and 16-row tile) but every token group re-reads
+// the weights, so it is the M <= 16 path.
 cudaError_t launch_gemm_skinny(const uint8_t* q, const float* sa, const uint8_t* w, const float* sw, int M,
                                int N, int K, void* out, bool out_f32, int num_sms, cudaStream_t stream);
 // The same with an explicit load depth per warp (1, 2 or 4 K blocks per step).
